@@ -1,0 +1,485 @@
+#!/usr/bin/env python3
+"""Benchmark: paged decode attention + gather_cached_kv on one GB300.
+
+One step is one pass of the whole hot path over one batch: a decode-attention
+call (split-context partitions + log-sum-exp merge when the plan splits) and a
+gather_cached_kv call.  Default workload: the LLaMA-13B-shaped MHA decode of
+"Optimizes the single_query_cached_kv_attention kernel" (8 sequences x 40
+heads, head_size 128, block_size 16, context 256, fp16, 2048-block pool) and
+the largest point of the gather sweep of "Memcpy kernel for flash attention"
+(2048 tokens, 40 heads, head_size 128, block_size 8, 1024 blocks, fp16).
+
+Prints ONE JSON line (rank 0).  `value` is algorithmic HBM bytes per step
+divided by device time per step (GB/s, 1e9).  Inputs rotate over enough
+device copies that every step reads data not left in L2 by the last one.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkd|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+# The CPU oracle legs run single-threaded; set before NumPy loads its BLAS.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+METRIC = ("paged decode attn µs/call and achieved HBM GB/s (% of GB300 roofline) "
+          "vs oracle")
+WORKLOAD = "llama13b_mha_b8_ctx256 decode + gather_t2048"
+DECODE_CFG = "llama13b_mha_b8_ctx256"
+GATHER_CFG = "gather_t2048"
+TARGETS = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "gqa_ctx4096_b256"]
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by
+# the sha256 (first 16 hex digits) of the kernel source it was taken on; the
+# value is reported only while that source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+# ---------------------------------------------------------------- byte counts
+
+def decode_bytes(c) -> int:
+    """Algorithmic HBM bytes of one decode call: K+V rows read, q read, out
+    written, block-table entries and context lengths read."""
+    e = 2
+    lens = [int(x) for x in c.context_lens]
+    kv = sum(lens) * c.num_kv_heads * c.head_size * 2 * e
+    qo = 2 * c.num_seqs * c.num_heads * c.head_size * e
+    tables = 4 * sum(-(-L // c.block_size) for L in lens) + 4 * c.num_seqs
+    return kv + qo + tables
+
+
+def gather_bytes(g) -> int:
+    """K and V rows read and written once each, plus the slot mapping."""
+    return 2 * 2 * g.num_tokens * g.num_heads * g.head_size * 2 + 8 * g.num_tokens
+
+
+def src_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        busy = [v for v in sm if mx and v >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- reference arm (oracle)
+
+def _oracle_sample(c, g, n):
+    """The first n units of the step: unit i = decode of (sequence i // H, head
+    i % H) over its whole context plus gather of 16 tokens."""
+    from oracle.gather import gather_cached_kv as ref_gather
+    from oracle.paged_attention import paged_decode_attention as ref_attn
+    H = c.num_heads
+    pairs = [(i // H, i % H) for i in range(n)]
+    tokens = g.slot_mapping[: min(g.num_tokens, 16 * n)]
+    per_pair = decode_bytes(c) / (c.num_seqs * H)
+    nbytes = per_pair * n + gather_bytes(g) * len(tokens) / g.num_tokens
+
+    def run():
+        ref_attn(c.q, c.key_cache, c.value_cache, c.block_tables, c.context_lens, c.scale,
+                 c.dtype, pairs=pairs)
+        ref_gather(g.key_cache, g.value_cache, tokens)
+    return run, nbytes, f"decode (seq, head) pairs 0..{n - 1} of {c.num_seqs * H} + " \
+                        f"gather tokens 0..{len(tokens) - 1} of {g.num_tokens}"
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, timed on the host cores, as the reference arm."""
+    if rank != 0:
+        return 0
+    from paged_kv_decode_22_gb300.workloads import (decode_configs, gather_sweep,
+                                                    make_decode_case, make_gather_case)
+    c = make_decode_case(name=DECODE_CFG, **decode_configs()[DECODE_CFG])
+    g = make_gather_case(name=GATHER_CFG, **gather_sweep()[GATHER_CFG])
+    full = c.num_seqs * c.num_heads
+    # Size the per-step sample so that warm-up + timed steps take about 60 s.
+    run1, _, _ = _oracle_sample(c, g, 1)
+    t0 = time.perf_counter()
+    for _ in range(5):
+        run1()
+    t_unit = (time.perf_counter() - t0) / 5
+    n = int(max(1, min(full, 60.0 / max(1, args.steps + args.warmup) / t_unit)))
+    run, nbytes, what = _oracle_sample(c, g, n)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) fp16 inputs, random non-overlapping block tables)",
+        "config": {"workload": WORKLOAD, "sample": what},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": what},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def cpu_baseline(c, g, budget_s=10.0):
+    """The oracle as it stands on the host, on a bounded sample of the step."""
+    run, nbytes, what = _oracle_sample(c, g, 16)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(nbytes * n / el / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "sample": f"{what}; {n} passes in {el:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
+    ap.add_argument("--no-targets", action="store_true", help="skip the large-batch GQA lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local = env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        # Only rank 0 times the oracle; other ranks exit without work.
+        return run_reference(args, world, rank)
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_22_gb300 import ops
+    from paged_kv_decode_22_gb300.workloads import (decode_configs, gather_sweep,
+                                                    make_decode_case, make_gather_case)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    c = make_decode_case(name=DECODE_CFG, **decode_configs()[DECODE_CFG])
+    g = make_gather_case(name=GATHER_CFG, **gather_sweep()[GATHER_CFG])
+    f16 = torch.float16
+
+    def upd(a, dt=None):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                             else np.ascontiguousarray(a))
+        return (t.view(dt) if dt is not None else t).to(dev)
+
+    step_bytes = decode_bytes(c) + gather_bytes(g)
+    # Rotation: enough independent device copies of every input and output
+    # that consecutive steps never find their data in L2 (touched bytes x
+    # copies > 3 x L2).
+    ncopy = max(2, math.ceil(3 * L2_BYTES / step_bytes))
+    sets = []
+    for _ in range(ncopy):
+        sets.append(dict(q=upd(c.q, f16), kc=upd(c.key_cache, f16), vc=upd(c.value_cache, f16),
+                         bt=upd(c.block_tables), cl=upd(c.context_lens),
+                         gkc=upd(g.key_cache, f16), gvc=upd(g.value_cache, f16),
+                         slots=upd(g.slot_mapping),
+                         out=torch.empty(c.q.shape, dtype=f16, device=dev),
+                         ko=torch.empty((g.num_tokens, g.num_heads, g.head_size), dtype=f16,
+                                        device=dev),
+                         vo=torch.empty((g.num_tokens, g.num_heads, g.head_size), dtype=f16,
+                                        device=dev)))
+    S, H, D = c.q.shape
+    ps, npart, path, ws_bytes = ops.decode_plan(S, H, c.num_kv_heads, D, c.block_size,
+                                                c.max_context_len)
+    work = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def decode_call(i, st=None):
+        d = sets[i % ncopy]
+        ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"], d["cl"],
+                                   c.max_context_len, c.scale, workspace=work, stream=st)
+
+    def gather_call(i, st=None):
+        d = sets[i % ncopy]
+        ops.gather_cached_kv(d["ko"], d["vo"], d["gkc"], d["gvc"], d["slots"], stream=st)
+
+    launches_per_step = 2 + (1 if npart > 1 else 0)
+    for i in range(args.warmup):
+        decode_call(i, stream)
+        gather_call(i, stream)
+    barrier()
+
+    # The timed steps replay CUDA graphs of CHUNK decode calls followed by CHUNK
+    # gather calls (inputs rotating over the device copies), so host launch
+    # overhead stays out of the device time.  Events between the two graphs
+    # give each kernel's average duration inside the same timed region.
+    CHUNK = 64
+
+    def capture(fn, n):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(n):
+                fn(i)
+        return gr
+
+    full, rest = divmod(args.steps, CHUNK)
+    graphs = [(capture(decode_call, CHUNK), capture(gather_call, CHUNK))] if full else []
+    tail = (capture(decode_call, rest), capture(gather_call, rest)) if rest else None
+    plan = [graphs[0]] * full + ([tail] if tail else [])
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    for gd, gg in plan[:2]:
+        gd.replay()
+        gg.replay()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(plan) + 1)]
+    with ClockSampler(gpu_id) as clocks:
+        barrier()
+        evs[0].record(stream)
+        for j, (gd, gg) in enumerate(plan):
+            gd.replay()
+            evs[2 * j + 1].record(stream)
+            gg.replay()
+            evs[2 * j + 2].record(stream)
+        barrier()
+    total_ms = evs[0].elapsed_time(evs[-1])
+    dec_ms = sum(evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(len(plan)))
+    gat_ms = sum(evs[2 * j + 1].elapsed_time(evs[2 * j + 2]) for j in range(len(plan)))
+    ms = total_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    dec_us = dec_ms * 1e3 / args.steps
+    gat_us = gat_ms * 1e3 / args.steps
+    del graphs, tail, plan
+
+    # End to end through the public API with host buffers: per step, copy the
+    # step's inputs (q, block tables, context lengths, slot mapping) from
+    # pinned host memory, run both calls, read every output back to pinned host
+    # memory.  The KV pools are resident state, as in serving.
+    hq = torch.from_numpy(c.q.view(np.int16)).view(f16).pin_memory()
+    hbt = torch.from_numpy(c.block_tables).pin_memory()
+    hcl = torch.from_numpy(c.context_lens).pin_memory()
+    hsl = torch.from_numpy(g.slot_mapping).pin_memory()
+    hout = torch.empty(sets[0]["out"].shape, dtype=f16).pin_memory()
+    hko = torch.empty(sets[0]["ko"].shape, dtype=f16).pin_memory()
+    hvo = torch.empty(sets[0]["vo"].shape, dtype=f16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hcl, hsl))
+    d2h = sum(t.numel() * t.element_size() for t in (hout, hko, hvo))
+
+    def e2e_step(i):
+        d = sets[i % ncopy]
+        d["q"].copy_(hq, non_blocking=True)
+        d["bt"].copy_(hbt, non_blocking=True)
+        d["cl"].copy_(hcl, non_blocking=True)
+        d["slots"].copy_(hsl, non_blocking=True)
+        decode_call(i, stream)
+        gather_call(i, stream)
+        hout.copy_(d["out"], non_blocking=True)
+        hko.copy_(d["ko"], non_blocking=True)
+        hvo.copy_(d["vo"], non_blocking=True)
+        stream.synchronize()
+
+    e2e_steps = max(20, min(2000, args.steps // 10))
+    for i in range(5):
+        e2e_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    barrier()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+
+    # Large-batch GQA lines (decode alone), inputs generated on the device
+    # from a seeded torch generator; timing does not depend on the values.
+    targets = {}
+    if not args.no_targets:
+        gen = torch.Generator(device=dev)
+        for name in TARGETS:
+            cfg = decode_configs()[name]
+            gen.manual_seed(cfg["seed"])
+            Sx, Hx, Hkx, Dx, Bx = (cfg["num_seqs"], cfg["num_heads"], cfg["num_kv_heads"],
+                                   cfg["head_size"], cfg["block_size"])
+            Lx = cfg["context_lens"][0]
+            nbx = Sx * Lx // Bx
+            bf = torch.bfloat16
+            kcx = torch.randn((nbx, Bx, Hkx, Dx), generator=gen, device=dev, dtype=bf)
+            vcx = torch.randn((nbx, Bx, Hkx, Dx), generator=gen, device=dev, dtype=bf)
+            qx = torch.randn((Sx, Hx, Dx), generator=gen, device=dev, dtype=bf)
+            perm = torch.randperm(nbx, generator=gen, device=dev).to(torch.int32)
+            btx = perm.view(Sx, Lx // Bx).contiguous()
+            clx = torch.full((Sx,), Lx, dtype=torch.int32, device=dev)
+            outx = torch.empty_like(qx)
+            _, npx, pathx, wsx = ops.decode_plan(Sx, Hx, Hkx, Dx, Bx, Lx)
+            workx = torch.empty(max(wsx, 256), dtype=torch.uint8, device=dev)
+            scale = 1.0 / math.sqrt(Dx)
+            nbytes = Sx * Lx * Hkx * Dx * 2 * 2 + 2 * Sx * Hx * Dx * 2 + 4 * Sx * (Lx // Bx) + 4 * Sx
+            flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+            def call():
+                ops.paged_decode_attention(outx, qx, kcx, vcx, btx, clx, Lx, scale,
+                                           workspace=workx, stream=stream)
+            for _ in range(3):
+                call()
+            times = []
+            for _ in range(20):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3)
+            us = statistics.median(times)
+            targets[name] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                             "path": "tc" if pathx == 1 else "simt", "partitions": npx}
+            del kcx, vcx, flush
+            torch.cuda.empty_cache()
+
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    if os.path.exists(peaks_path):
+        with open(peaks_path) as f:
+            pk = json.load(f)
+        if pk.get("hbm_gbs"):
+            peak, peak_src = float(pk["hbm_gbs"]), "measured"
+    for v in targets.values():
+        v["frac"] = round(v["GBps"] / peak, 3)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    dec_b, gat_b = decode_bytes(c), gather_bytes(g)
+    if dec_us >= gat_us:
+        dom, dom_bytes, dom_us, dom_src = "decode", dec_b, dec_us, ("paged_kv_decode_22_gb300/csrc/decode_simt.cu",)
+    else:
+        dom, dom_bytes, dom_us, dom_src = "gather_cached_kv", gat_b, gat_us, ("paged_kv_decode_22_gb300/csrc/copy_kv.cu",)
+    achieved = dom_bytes / dom_us / 1e3
+    traffic = NCU_TRAFFIC.get(src_hash(*dom_src))
+    value = step_bytes * world / ms / 1e6
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "data": "synthetic (seeded N(0,1) fp16, random non-overlapping block tables)",
+        "config": {"workload": WORKLOAD, "decode": "S=8 H=40 Hk=40 D=128 B=16 ctx=256 NB=2048",
+                   "gather": "T=2048 H=40 D=128 B=8 NB=1024",
+                   "l2": f"inputs rotate over {ncopy} device copies (>3x L2 touched per cycle)",
+                   "decode_partitions": npart, "decode_path": "tc" if path == 1 else "simt"},
+        "decode_us_per_call": round(dec_us, 2), "gather_us_per_call": round(gat_us, 2),
+        "step_bytes": step_bytes,
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes},
+        "e2e": {"value": round(step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+        "targets_decode_bf16_gqa64x8": targets,
+    }
+    if world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(c, g)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

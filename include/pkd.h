@@ -1,0 +1,178 @@
+/*
+ * pkd.h -- C ABI of the GB300 (sm_103a) paged-KV decode attention library.
+ *
+ * Operations (all from the vLLM pull-request pages the library is built on):
+ *
+ *  - pkd_paged_decode_attention: decode-phase attention over a paged KV
+ *    cache, the operation vLLM calls single_query_cached_kv_attention
+ *    ("Optimizes the single_query_cached_kv_attention kernel", pull request
+ *    420).  For every sequence s and query head h,
+ *        out[s,h,:] = softmax_t(scale * q[s,h,:] . K_s[t,:]) @ V_s[t,:]
+ *    over t < context_lens[s], where
+ *        K_s[t] = key_cache[block_tables[s, t / block_size], t % block_size, kv(h), :]
+ *    and kv(h) = h / (num_heads / num_kv_heads): contiguous groups of query
+ *    heads share one KV head, as in the head mapping of "Optimize MQA
+ *    Kernel" (pull request 452), so MHA, GQA and MQA are one call.  Long
+ *    contexts at small batch are cut into partitions whose partial results
+ *    are merged by a log-sum-exp reduction (the split-context form behind
+ *    the "Paged attention V2" column of the kernel-latency tables in
+ *    "[Performance] Support MQA/GQA in decode phase by using
+ *    FlashAttention", pull request 2744).
+ *
+ *  - pkd_gather_cached_kv: copies the cached K/V rows of the slots listed in
+ *    a slot mapping into contiguous [num_tokens, num_heads, head_size]
+ *    tensors ("Memcpy kernel for flash attention", pull request 29).
+ *
+ *  - pkd_reshape_and_cache: the inverse copy, storing new tokens' K/V rows
+ *    into their cache slots (the cache_ops.cache step named in the notes of
+ *    pull request 2744).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor argument is a DEVICE pointer owned by the caller, dense
+ *    row-major (C order), 16-byte aligned.  16-bit values are IEEE binary16
+ *    (PKD_FP16) or bfloat16 (PKD_BF16) bit patterns.
+ *  - Cache layout: key_cache and value_cache are
+ *    [num_blocks][block_size][num_kv_heads][head_size].  A slot is
+ *    block_id * block_size + offset.
+ *  - The library allocates no memory and never synchronises the host.  Work
+ *    is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream) in stream order.
+ *  - Host-detectable errors return a status before anything is launched.
+ *    PKD_ERR_CUDA means a launch failed; pkd_last_error() describes it.
+ *  - Data-dependent errors (bad block ids, slots or lengths) cannot be seen
+ *    on the host; kernels OR a PKD_DEV_* bit into *device_status (a device
+ *    uint32_t, may be NULL) and write the documented fallback output.  The
+ *    caller reads the word back whenever it chooses.
+ */
+#ifndef PKD_H_
+#define PKD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKD_API __attribute__((visibility("default")))
+#else
+#define PKD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkd_status {
+  PKD_OK = 0,
+  PKD_ERR_NULL = 1,         /* a required pointer is NULL */
+  PKD_ERR_SHAPE = 2,        /* sizes inconsistent or out of range */
+  PKD_ERR_UNSUPPORTED = 3,  /* head_size / block_size / dtype not compiled in */
+  PKD_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+  PKD_ERR_ALIGN = 5,        /* a tensor pointer is not 16-byte aligned */
+  PKD_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
+  PKD_ERR_DEVICE = 7        /* the current device is not an sm_103 GPU */
+} pkd_status;
+
+typedef enum pkd_dtype { PKD_FP16 = 0, PKD_BF16 = 1 } pkd_dtype;
+
+/* Bits OR-ed into *device_status by the kernels. */
+#define PKD_DEV_BAD_BLOCK 1u /* a referenced block id is outside [0, num_blocks) */
+#define PKD_DEV_BAD_SLOT 2u  /* a slot is outside [0, num_blocks * block_size) */
+#define PKD_DEV_BAD_LEN 4u   /* context_lens[s] < 0, > max_context_len or > table */
+#define PKD_DEV_TIMEOUT 8u   /* a bounded wait inside a kernel gave up */
+
+/* Decode kernel families, as reported by pkd_decode_plan(). */
+#define PKD_PATH_SIMT 0   /* CUDA-core path (query-group size below 4) */
+#define PKD_PATH_TC 1     /* tcgen05 tensor-core path with TMA staging */
+
+/*
+ * Launch plan of pkd_paged_decode_attention for the given sizes on the
+ * CURRENT device (same size rules as that call).  partition_size = 0 lets
+ * the library choose; a positive value (a multiple of 64 tokens) forces
+ * that partition length.  Outputs
+ * (any may be NULL): the partition length in tokens, the number of
+ * partitions (1 = no split, no reduction launch), the kernel family, and the
+ * workspace bytes the call needs (0 when unsplit).  Pure host arithmetic
+ * plus a cached device-attribute query; allocates nothing.
+ */
+PKD_API pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                           int block_size, int max_context_len, int partition_size,
+                           int* out_partition_size, int* out_num_partitions, int* out_path,
+                           size_t* out_workspace_bytes);
+
+/*
+ * Decode attention over a paged KV cache.
+ *   out           [num_seqs][num_heads][head_size]            16-bit, written
+ *   q             [num_seqs][num_heads][head_size]            16-bit
+ *   key_cache,
+ *   value_cache   [num_blocks][block_size][num_kv_heads][head_size] 16-bit
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32; entries past
+ *                 ceil(context_lens[s] / block_size) are never read
+ *   context_lens  [num_seqs] int32, each in [0, max_context_len]
+ *   max_context_len  host-side upper bound of context_lens (sizes the grid)
+ *   num_heads % num_kv_heads == 0;  head_size in {64, 128};
+ *   block_size a power of two in [8, 256];  1 <= num_seqs <= 65535
+ *   scale         logit multiplier (1/sqrt(head_size) for standard attention)
+ *   partition_size  0 = library choice, else a multiple of 64 tokens
+ *   workspace     device scratch of >= the plan's workspace bytes (may be
+ *                 NULL when the plan has one partition); its contents on
+ *                 entry do not matter and are clobbered
+ *   device_status optional device uint32_t for PKD_DEV_* bits
+ * Results are rounded to nearest-even from fp32 accumulation.  A sequence
+ * with context_lens[s] == 0 yields zeros.  A sequence with an invalid length
+ * or a referenced block id outside [0, num_blocks) yields zeros and sets the
+ * matching PKD_DEV_* bit.
+ */
+PKD_API pkd_status pkd_paged_decode_attention(void* out, const void* q, const void* key_cache,
+                                      const void* value_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens,
+                                      int max_context_len, int num_seqs, int num_heads,
+                                      int num_kv_heads, int head_size, int block_size,
+                                      int num_blocks, float scale, pkd_dtype dtype,
+                                      int partition_size, void* workspace,
+                                      size_t workspace_bytes, uint32_t* device_status,
+                                      void* stream);
+
+/*
+ * gather_cached_kv: key_out[t] = key_cache[slot / block_size][slot % block_size]
+ * and value_out[t] likewise, slot = slot_mapping[t], bit for bit.
+ *   key_out, value_out        [num_tokens][num_heads][head_size] 16-bit, written
+ *   key_cache, value_cache    [num_blocks][block_size][num_heads][head_size]
+ *   slot_mapping              [num_tokens] int64
+ * num_tokens may be 0 (nothing is launched).  A slot outside
+ * [0, num_blocks * block_size) gives zero rows and sets PKD_DEV_BAD_SLOT.
+ * head_size must be a multiple of 8; any block_size >= 1.
+ */
+PKD_API pkd_status pkd_gather_cached_kv(void* key_out, void* value_out, const void* key_cache,
+                                const void* value_cache, const int64_t* slot_mapping,
+                                int num_tokens, int num_heads, int head_size, int block_size,
+                                int num_blocks, pkd_dtype dtype, uint32_t* device_status,
+                                void* stream);
+
+/*
+ * reshape_and_cache: key_cache[slot / block_size][slot % block_size] = key[t]
+ * and the same for value, slot = slot_mapping[t], bit for bit.
+ *   key, value                [num_tokens][num_heads][head_size] 16-bit
+ *   key_cache, value_cache    [num_blocks][block_size][num_heads][head_size], updated
+ *   slot_mapping              [num_tokens] int64
+ * A negative slot marks a token that is not stored (no status bit).  A slot
+ * at or past num_blocks * block_size is not stored and sets PKD_DEV_BAD_SLOT.
+ * Two tokens with the same slot race; the caller must not do that.
+ */
+PKD_API pkd_status pkd_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                 void* value_cache, const int64_t* slot_mapping, int num_tokens,
+                                 int num_heads, int head_size, int block_size, int num_blocks,
+                                 pkd_dtype dtype, uint32_t* device_status, void* stream);
+
+/* Static text for a status code. */
+PKD_API const char* pkd_status_string(pkd_status status);
+
+/* Text of the last PKD_ERR_CUDA raised on this host thread ("" if none). */
+PKD_API const char* pkd_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+PKD_API int pkd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKD_H_ */

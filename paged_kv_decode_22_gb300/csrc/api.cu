@@ -1,0 +1,252 @@
+// C ABI of the library (declared in include/pkd.h): argument validation,
+// launch planning and dispatch.  Allocates nothing and never synchronises.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/pkd.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+pkd_status cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return PKD_ERR_CUDA;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0;
+  int minor = 0;
+};
+
+// Per-device attributes, queried once per device and cached.
+pkd_status device_info(DeviceInfo* out) {
+  static DeviceInfo cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return PKD_ERR_DEVICE;
+  DeviceInfo& d = cache[dev];
+  if (d.sms == 0) {
+    DeviceInfo n;
+    if ((e = cudaDeviceGetAttribute(&n.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d = n;
+  }
+  *out = d;
+  if (d.major != 10 || d.minor != 3) return PKD_ERR_DEVICE;  // built for sm_103a only
+  return PKD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+constexpr int kPartitionQuantum = 64;   // partitions are whole 64-token tiles
+constexpr int kTargetCtasPerSm = 4;     // split until about this many CTAs per SM
+
+struct Plan {
+  int partition_size = kPartitionQuantum;
+  int num_partitions = 1;
+  int path = PKD_PATH_SIMT;
+  size_t ws_bytes = 0;
+  size_t off_m = 0, off_l = 0;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+pkd_status check_decode_sizes(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                              int max_context_len) {
+  if (num_seqs < 1 || num_seqs > 65535 || num_heads < 1 || num_kv_heads < 1 ||
+      max_context_len < 0)
+    return PKD_ERR_SHAPE;
+  if (num_heads % num_kv_heads != 0) return PKD_ERR_SHAPE;
+  if (num_kv_heads * (num_heads / num_kv_heads) > 65535) return PKD_ERR_SHAPE;
+  if (head_size != 64 && head_size != 128) return PKD_ERR_UNSUPPORTED;
+  return PKD_OK;
+}
+
+pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                     int max_context_len, int block_size, int partition_size, Plan* plan) {
+  pkd_status st = check_decode_sizes(num_seqs, num_heads, num_kv_heads, head_size, max_context_len);
+  if (st != PKD_OK) return st;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != PKD_OK) return st;
+  const int g = num_heads / num_kv_heads;
+  Plan p;
+  p.path = pkd::decode_tc_supported(head_size, g, block_size) ? PKD_PATH_TC : PKD_PATH_SIMT;
+  const long long units = (long long)num_seqs * num_kv_heads *
+                          (p.path == PKD_PATH_SIMT ? g / pkd::simt_heads_per_cta(g) : 1);
+  const int max_tiles = std::max(1, (max_context_len + kPartitionQuantum - 1) / kPartitionQuantum);
+  if (partition_size > 0) {
+    if (partition_size % kPartitionQuantum) return PKD_ERR_SHAPE;
+    p.partition_size = partition_size;
+  } else {
+    const long long target = (long long)kTargetCtasPerSm * dev.sms;
+    long long parts = units >= target ? 1 : (target + units - 1) / units;
+    parts = std::min<long long>(parts, max_tiles);
+    const int tiles = (int)((max_tiles + parts - 1) / parts);
+    p.partition_size = tiles * kPartitionQuantum;
+  }
+  p.num_partitions = std::max(1, (max_context_len + p.partition_size - 1) / p.partition_size);
+  if (p.num_partitions > 65535) return PKD_ERR_SHAPE;
+  if (p.num_partitions > 1) {
+    const size_t rows = (size_t)num_seqs * num_heads * p.num_partitions;
+    p.off_m = align256(rows * head_size * sizeof(float));
+    p.off_l = p.off_m + align256(rows * sizeof(float));
+    p.ws_bytes = p.off_l + align256(rows * sizeof(float));
+  }
+  *plan = p;
+  return PKD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                           int block_size, int max_context_len, int partition_size,
+                           int* out_partition_size, int* out_num_partitions, int* out_path,
+                           size_t* out_workspace_bytes) {
+  if (!pow2_in(block_size, 8, 256)) return PKD_ERR_UNSUPPORTED;
+  Plan p;
+  pkd_status st = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_context_len,
+                            block_size, partition_size, &p);
+  if (st != PKD_OK) return st;
+  if (out_partition_size) *out_partition_size = p.partition_size;
+  if (out_num_partitions) *out_num_partitions = p.num_partitions;
+  if (out_path) *out_path = p.path;
+  if (out_workspace_bytes) *out_workspace_bytes = p.ws_bytes;
+  return PKD_OK;
+}
+
+pkd_status pkd_paged_decode_attention(void* out, const void* q, const void* key_cache,
+                                      const void* value_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens,
+                                      int max_context_len, int num_seqs, int num_heads,
+                                      int num_kv_heads, int head_size, int block_size,
+                                      int num_blocks, float scale, pkd_dtype dtype,
+                                      int partition_size, void* workspace,
+                                      size_t workspace_bytes, uint32_t* device_status,
+                                      void* stream) {
+  if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
+    return PKD_ERR_NULL;
+  if (dtype != PKD_FP16 && dtype != PKD_BF16) return PKD_ERR_UNSUPPORTED;
+  if (!pow2_in(block_size, 8, 256)) return PKD_ERR_UNSUPPORTED;
+  if (num_blocks < 1 || max_blocks_per_seq < 1) return PKD_ERR_SHAPE;
+  if ((long long)num_blocks * block_size > 0x7fffffffLL) return PKD_ERR_SHAPE;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+    return PKD_ERR_ALIGN;
+  Plan plan;
+  pkd_status st = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_context_len,
+                            block_size, partition_size, &plan);
+  if (st != PKD_OK) return st;
+  if (plan.num_partitions > 1) {
+    if (!workspace || workspace_bytes < plan.ws_bytes) return PKD_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKD_ERR_ALIGN;
+  }
+
+  pkd::DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.is_bf16 = dtype == PKD_BF16;
+  a.partition_size = plan.partition_size;
+  a.num_partitions = plan.num_partitions;
+  char* ws = static_cast<char*>(workspace);
+  a.ws_o = plan.num_partitions > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+  a.ws_m = plan.num_partitions > 1 ? reinterpret_cast<float*>(ws + plan.off_m) : nullptr;
+  a.ws_l = plan.num_partitions > 1 ? reinterpret_cast<float*>(ws + plan.off_l) : nullptr;
+  a.status = device_status;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = plan.path == PKD_PATH_TC ? pkd::launch_decode_tc(a, s) : pkd::launch_decode_simt(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (plan.num_partitions > 1) {
+    e = pkd::launch_lse_reduce(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "lse_reduce launch");
+  }
+  return PKD_OK;
+}
+
+static pkd_status copy_common(const void* a, const void* b, const void* c, const void* d,
+                              const int64_t* slots, int num_tokens, int num_heads, int head_size,
+                              int block_size, int num_blocks, pkd_dtype dtype) {
+  if (num_tokens < 0 || num_heads < 1 || head_size < 8 || head_size % 8 || block_size < 1 ||
+      num_blocks < 1)
+    return PKD_ERR_SHAPE;
+  if (dtype != PKD_FP16 && dtype != PKD_BF16) return PKD_ERR_UNSUPPORTED;
+  if ((long long)num_heads * head_size > 0x7fffffffLL / 2) return PKD_ERR_SHAPE;
+  if (num_tokens == 0) return PKD_OK;
+  if (!a || !b || !c || !d || !slots) return PKD_ERR_NULL;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(d)) return PKD_ERR_ALIGN;
+  DeviceInfo dev;
+  return device_info(&dev);
+}
+
+pkd_status pkd_gather_cached_kv(void* key_out, void* value_out, const void* key_cache,
+                                const void* value_cache, const int64_t* slot_mapping,
+                                int num_tokens, int num_heads, int head_size, int block_size,
+                                int num_blocks, pkd_dtype dtype, uint32_t* device_status,
+                                void* stream) {
+  pkd_status st = copy_common(key_out, value_out, key_cache, value_cache, slot_mapping, num_tokens,
+                              num_heads, head_size, block_size, num_blocks, dtype);
+  if (st != PKD_OK || num_tokens == 0) return st;
+  pkd::CopyArgs a{key_out, value_out, key_cache, value_cache, slot_mapping, num_tokens,
+                  num_heads * head_size, block_size, num_blocks, device_status};
+  cudaError_t e = pkd::launch_gather(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKD_OK : cuda_fail(e, "gather launch");
+}
+
+pkd_status pkd_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                 void* value_cache, const int64_t* slot_mapping, int num_tokens,
+                                 int num_heads, int head_size, int block_size, int num_blocks,
+                                 pkd_dtype dtype, uint32_t* device_status, void* stream) {
+  pkd_status st = copy_common(key_cache, value_cache, key, value, slot_mapping, num_tokens,
+                              num_heads, head_size, block_size, num_blocks, dtype);
+  if (st != PKD_OK || num_tokens == 0) return st;
+  pkd::CopyArgs a{key_cache, value_cache, key, value, slot_mapping, num_tokens,
+                  num_heads * head_size, block_size, num_blocks, device_status};
+  cudaError_t e = pkd::launch_scatter(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKD_OK : cuda_fail(e, "reshape_and_cache launch");
+}
+
+const char* pkd_status_string(pkd_status status) {
+  switch (status) {
+    case PKD_OK: return "ok";
+    case PKD_ERR_NULL: return "a required pointer is NULL";
+    case PKD_ERR_SHAPE: return "sizes inconsistent or out of range";
+    case PKD_ERR_UNSUPPORTED: return "head_size, block_size or dtype not supported";
+    case PKD_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKD_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned (workspace: 256)";
+    case PKD_ERR_CUDA: return "a CUDA call or launch failed";
+    case PKD_ERR_DEVICE: return "current device is not an sm_103 GPU";
+  }
+  return "unknown status";
+}
+
+const char* pkd_last_error(void) { return g_last_error; }
+
+int pkd_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Device-side helpers shared by the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/pkd.h"
+
+namespace pkd {
+
+// Two 16-bit values packed in a 32-bit word, widened to float.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16) {
+    // bf16 is the top half of a binary32: widening is a shift, exact.
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(h);
+  }
+}
+
+// Round two floats to the 16-bit format (nearest-even) and pack them.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// 16-byte global load that bypasses L1 allocation (streamed data).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// 16-byte global store with the streaming (evict-first) hint.
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// A context length is usable when it fits the grid and the block table.
+__device__ __forceinline__ bool len_ok(int L, int max_context_len, int max_blocks_per_seq,
+                                       int block_size) {
+  return L >= 0 && L <= max_context_len &&
+         (long long)L <= (long long)max_blocks_per_seq * block_size;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace pkd

@@ -1,0 +1,58 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkd {
+
+// Arguments of one decode-attention launch, already validated on the host.
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* key_cache;
+  const void* value_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int max_blocks_per_seq;
+  int max_context_len;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int head_size;
+  int block_size;
+  int num_blocks;
+  float scale;
+  int is_bf16;
+  int partition_size;   // tokens per partition (multiple of 64)
+  int num_partitions;   // 1 = write `out` directly
+  float* ws_o;          // [S][H][P][D] unnormalised partial outputs
+  float* ws_m;          // [S][H][P] partial maxima (log2 domain)
+  float* ws_l;          // [S][H][P] partial sums; < 0 marks a bad block
+  uint32_t* status;
+};
+
+struct CopyArgs {
+  void* dst_k;
+  void* dst_v;
+  const void* src_k;
+  const void* src_v;
+  const int64_t* slots;
+  int num_tokens;
+  int row_elems;    // num_heads * head_size
+  int block_size;
+  int num_blocks;
+  uint32_t* status;
+};
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
+int simt_heads_per_cta(int group);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
+bool decode_tc_supported(int head_size, int group, int block_size);
+cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st);
+cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st);
+
+}  // namespace pkd
