@@ -61,13 +61,14 @@ def test_gather_empty_is_a_no_op():
                                          (3, 16, 3, "fp16")])
 def test_reshape_and_cache_bit_exact(H, D, B, dtype):
     from paged_kv_decode_22_gb300 import ops
+    nb = max(64, -(-400 // B))
     g = make_gather_case(seed=6, num_tokens=300, num_heads=H, head_size=D, block_size=B,
-                         num_blocks=64, dtype=dtype)
+                         num_blocks=nb, dtype=dtype)
     rng = np.random.default_rng(2)
     key = rng.integers(0, 0x7C00, (300, H, D), dtype=np.uint16)   # finite fp16/bf16 patterns
     val = rng.integers(0, 0x7C00, (300, H, D), dtype=np.uint16)
     slots = g.slot_mapping.copy()
-    slots[[0, 5]] = [-1, 64 * B + 2]
+    slots[[0, 5]] = [-1, nb * B + 2]
     kc, vc = up(g.key_cache, dtype), up(g.value_cache, dtype)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ops.reshape_and_cache(up(key, dtype), up(val, dtype), kc, vc, up(slots),
