@@ -74,27 +74,53 @@ pkd_status check_decode_sizes(int num_seqs, int num_heads, int num_kv_heads, int
   return PKD_OK;
 }
 
+// Tiles-per-CTA estimate of the persistent tensor-core kernel for P
+// partitions: CTAs take units round-robin, so the busiest CTA handles
+// ceil(units * P / ctas) units of ceil(tiles / P) tiles; each unit costs about
+// a quarter tile of fixed work and a split adds the merge launch.
+double tc_cost(long long units, int tiles, int P, int ctas) {
+  const long long per_cta = (units * P + ctas - 1) / ctas;
+  const int tiles_per_unit = (tiles + P - 1) / P;
+  return (double)per_cta * tiles_per_unit + 0.25 * per_cta + (P > 1 ? 2.0 : 0.0);
+}
+
 pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                      int max_context_len, int block_size, int partition_size, Plan* plan) {
   pkd_status st = check_decode_sizes(num_seqs, num_heads, num_kv_heads, head_size, max_context_len);
   if (st != PKD_OK) return st;
+  if (partition_size < 0) return PKD_ERR_SHAPE;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != PKD_OK) return st;
   const int g = num_heads / num_kv_heads;
   Plan p;
-  p.path = pkd::decode_tc_supported(head_size, g, block_size) ? PKD_PATH_TC : PKD_PATH_SIMT;
-  const long long units = (long long)num_seqs * num_kv_heads *
-                          (p.path == PKD_PATH_SIMT ? g / pkd::simt_heads_per_cta(g) : 1);
-  const int max_tiles = std::max(1, (max_context_len + kPartitionQuantum - 1) / kPartitionQuantum);
+  const int tc_tile = pkd::decode_tc_tile();
+  const bool tc = pkd::decode_tc_supported(head_size, g, block_size) &&
+                  (partition_size == 0 || partition_size % tc_tile == 0);
+  p.path = tc ? PKD_PATH_TC : PKD_PATH_SIMT;
+  const int quantum = tc ? tc_tile : kPartitionQuantum;
+  const int max_tiles = std::max(1, (max_context_len + quantum - 1) / quantum);
   if (partition_size > 0) {
     if (partition_size % kPartitionQuantum) return PKD_ERR_SHAPE;
     p.partition_size = partition_size;
+  } else if (tc) {
+    const long long units = (long long)num_seqs * num_kv_heads;
+    int best = 1;
+    double best_cost = tc_cost(units, max_tiles, 1, dev.sms);
+    for (int P = 2; P <= max_tiles && P <= 64; ++P) {
+      const double c = tc_cost(units, max_tiles, P, dev.sms);
+      if (c < best_cost * 0.97) {
+        best_cost = c;
+        best = P;
+      }
+    }
+    p.partition_size = ((max_tiles + best - 1) / best) * quantum;
   } else {
+    const long long units = (long long)num_seqs * num_kv_heads * (g / pkd::simt_heads_per_cta(g));
     const long long target = (long long)kTargetCtasPerSm * dev.sms;
     long long parts = units >= target ? 1 : (target + units - 1) / units;
     parts = std::min<long long>(parts, max_tiles);
     const int tiles = (int)((max_tiles + parts - 1) / parts);
-    p.partition_size = tiles * kPartitionQuantum;
+    p.partition_size = tiles * quantum;
   }
   p.num_partitions = std::max(1, (max_context_len + p.partition_size - 1) / p.partition_size);
   if (p.num_partitions > 65535) return PKD_ERR_SHAPE;

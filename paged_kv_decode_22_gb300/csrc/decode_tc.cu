@@ -1,11 +1,598 @@
-// Tensor-core decode path (tcgen05 + TMA).  Not compiled in yet: every
-// configuration takes the CUDA-core path.
+// Decode attention over a paged KV cache on the 5th-generation tensor cores
+// (tcgen05 MMA, accumulators in TMEM), K/V staged by TMA.  Used when a KV head
+// is shared by 4..64 query heads (GQA / MQA) with head_size 128: then
+// q K^T and p V are real dense contractions of a tile of 128 cached tokens
+// against the whole query group, which is why the group sharing of
+// "Optimize MQA Kernel" (vLLM pull request 452) and the GQA case of
+// "[Performance] Support MQA/GQA in decode phase by using FlashAttention"
+// (pull request 2744) map onto them.
+//
+// Work unit = (sequence s, KV head, context partition).  A persistent grid of
+// one CTA per SM walks its units round-robin; inside the CTA, warps are
+// specialised and linked by mbarriers so the K/V stream never stops at unit
+// boundaries:
+//   warp 0     producer: reads block ids, issues TMA loads of q (per unit)
+//              and of K and V tiles (128 tokens) into rings of 32 KB stages.
+//              Blocks past the partition end (and out-of-range ids) are
+//              loaded from an out-of-bounds coordinate, which TMA fills with
+//              zeros without touching memory.
+//   warp 1     MMA issuer (one thread): S^T = K q^T (M = 128 tokens,
+//              N = group padded to 16) into TMEM, then O^T = V^T P^T
+//              (M = 128 = head_size, K = 128 tokens).
+//   warps 2-5  softmax / epilogue (thread = TMEM lane = token row of S and
+//              d row of O): online softmax with per-tile maxima shared
+//              through shared memory, P written (16-bit) for the second MMA,
+//              O accumulated in registers with the running rescale, and the
+//              final (or partial, for split context) result written.
+// Shared-memory operands use the 128-byte swizzled canonical layouts: K, q and
+// P K-major, V MN-major (head_size contiguous).
+#include <cuda.h>
+
+#include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace pkd {
+namespace {
 
-bool decode_tc_supported(int, int, int) { return false; }
+using namespace sm100;
 
-cudaError_t launch_decode_tc(const DecodeArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int TT = 128;                 // tokens per tile (= MMA M for S)
+constexpr int HD = 128;                 // head_size of this path (= MMA M for O)
+constexpr int TILE_BYTES = TT * HD * 2; // one K or V tile, 32 KB
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr uint32_t kSoftmaxBar = 1;     // named barrier id of warps 2-5
+
+__host__ __device__ constexpr int k_stages(int npad) { return npad <= 48 ? 3 : 2; }
+__host__ __device__ constexpr int v_stages(int npad) { return npad <= 16 ? 3 : 2; }
+__host__ __device__ constexpr int tmem_cols(int npad) {
+  return 4 * npad <= 32 ? 32 : 4 * npad <= 64 ? 64 : 4 * npad <= 128 ? 128 : 256;
+}
+
+template <int NPAD>
+struct SmemLayout {
+  static constexpr int NK = k_stages(NPAD);
+  static constexpr int NV = v_stages(NPAD);
+  static constexpr int QB = NPAD * HD * 2;   // one q (or P) buffer
+  static constexpr int off_k = 0;
+  static constexpr int off_v = off_k + NK * TILE_BYTES;
+  static constexpr int off_q = off_v + NV * TILE_BYTES;
+  static constexpr int off_p = off_q + 2 * QB;
+  static constexpr int off_misc = off_p + 2 * QB;
+  static constexpr int misc_bytes = 4608;
+  static constexpr int bytes = off_misc + misc_bytes;
+};
+
+struct Misc {
+  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+  uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], drain;
+  uint32_t tmem_base;
+  int abort;
+  int k_bad[3];                 // per K stage: the tile referenced a bad block id
+  float red[2][4][64];          // per-warp tile maxima
+  float m_run[64];              // running maxima (log2 domain)
+  float alpha[2][64];           // rescale factor of each tile parity
+  float lsum[4][64];            // per-warp exponent sums at finalisation
+};
+
+static_assert(sizeof(Misc) <= SmemLayout<16>::misc_bytes, "misc area too small");
+
+struct UnitInfo {
+  int s, hk, p, L, t0, t1, ntiles;
+  bool lok;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
+  UnitInfo ui;
+  const int P = a.num_partitions;
+  ui.p = u % P;
+  const int sh = u / P;
+  ui.hk = sh % a.num_kv_heads;
+  ui.s = sh / a.num_kv_heads;
+  ui.L = a.context_lens[ui.s];
+  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
+  ui.t0 = ui.p * a.partition_size;
+  ui.t1 = min(ui.t0 + a.partition_size, ui.L);
+  ui.ntiles = (ui.lok && ui.t0 < ui.L) ? (ui.t1 - ui.t0 + TT - 1) / TT : 0;
+  return ui;
+}
+
+__device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
+  ms.abort = 1;
+  flag(status, PKD_DEV_TIMEOUT);
+}
+
+// Position of element (row r, 16-bit column c) inside a K-major operand made
+// of 128-byte swizzled slabs of 64 columns, `rows` rows per slab.
+__device__ __forceinline__ int sw128_offset(int r, int c, int rows) {
+  return (c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <bool BF16, int NPAD>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
+  using LY = SmemLayout<NPAD>;
+  constexpr int NK = LY::NK, NV = LY::NV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  uint8_t* kbuf = sm + LY::off_k;
+  uint8_t* vbuf = sm + LY::off_v;
+  uint8_t* qbuf = sm + LY::off_q;
+  uint8_t* pbuf = sm + LY::off_p;
+  Misc& ms = *reinterpret_cast<Misc*>(sm + LY::off_misc);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = a.num_heads / a.num_kv_heads;
+  const int n_units = a.num_seqs * a.num_kv_heads * a.num_partitions;
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&ms.k_full[i], 1);
+      mbar_init(&ms.k_empty[i], 1 + kSoftmaxThreads);
+      ms.k_bad[i] = 0;
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&ms.v_full[i], 1);
+      mbar_init(&ms.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms.q_full[i], 1);
+      mbar_init(&ms.q_empty[i], 1);
+      mbar_init(&ms.s_full[i], 1);
+      mbar_init(&ms.p_full[i], kSoftmaxThreads);
+      mbar_init(&ms.o_full[i], 1);
+    }
+    mbar_init(&ms.drain, 1);
+    ms.abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&qmap);
+  }
+  // P buffers start at zero: rows of padded heads are never written again.
+  for (int i = threadIdx.x; i < 2 * LY::QB / 16; i += kThreads)
+    reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < 64; i += kThreads) ms.m_run[i] = -INFINITY;
+  if (warp == 1) {
+    tmem_alloc(&ms.tmem_base, tmem_cols(NPAD));
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+
+  if (warp == 0) {
+    // ============================================================ producer
+    const int B = a.block_size;
+    const int R = B < TT ? B : TT;            // rows per TMA box
+    const int nbox = TT / R;                  // boxes per tile and 64-column half
+    const int oob_row = a.num_blocks * B;     // first row past the pool: zero fill
+    const uint64_t policy = policy_evict_first();
+    uint32_t jk = 0, un = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const UnitInfo ui = unit_info(a, u);
+      if (ui.ntiles == 0) continue;
+      const int32_t* bt = a.block_tables + (size_t)ui.s * a.max_blocks_per_seq;
+      if (lane == 0) {
+        const int qb = un & 1;
+        ok = mbar_wait(&ms.q_empty[qb], ((un >> 1) & 1) ^ 1);
+        if (ok) {
+          mbar_arrive_expect_tx(&ms.q_full[qb], LY::QB);
+          const int row0 = ui.s * a.num_heads + ui.hk * g;
+          tma_load_2d(qbuf + qb * LY::QB, &qmap, &ms.q_full[qb], 0, row0);
+          tma_load_2d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, row0);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // Block ids of the first tile; later tiles are fetched one tile ahead.
+      auto fetch = [&](int jl, int& row, bool& bad) {
+        const int ts = ui.t0 + jl * TT;
+        row = oob_row;
+        bad = false;
+        if (lane < nbox) {
+          const int tok0 = B <= TT ? ts + lane * B : ts;
+          if (tok0 < ui.t1) {
+            const int id = __ldg(bt + tok0 / B);
+            if (id >= 0 && id < a.num_blocks)
+              row = id * B + (B <= TT ? 0 : (ts % B));
+            else
+              bad = true;
+          }
+        }
+      };
+      int row, nrow;
+      bool bad, nbad;
+      fetch(0, row, bad);
+      for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++jk) {
+        if (jl + 1 < ui.ntiles) fetch(jl + 1, nrow, nbad);
+        const bool any_bad = __any_sync(0xffffffffu, bad);
+        if (any_bad && lane == 0) flag(a.status, PKD_DEV_BAD_BLOCK);
+        const int ks = jk % NK, vs = jk % NV;
+        if (lane == 0) {
+          ok = mbar_wait(&ms.k_empty[ks], ((jk / NK) & 1) ^ 1);
+          if (ok) {
+            ms.k_bad[ks] = any_bad ? 1 : 0;
+            mbar_arrive_expect_tx(&ms.k_full[ks], TILE_BYTES);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        for (int i = 0; i < nbox; ++i) {
+          const int r = __shfl_sync(0xffffffffu, row, i);
+          if (lane == 0) {
+            uint8_t* dst = kbuf + ks * TILE_BYTES + i * R * 128;
+            tma_load_3d_hint(dst, &kmap, &ms.k_full[ks], 0, ui.hk, r, policy);
+            tma_load_3d_hint(dst + TT * 128, &kmap, &ms.k_full[ks], 64, ui.hk, r, policy);
+          }
+        }
+        if (lane == 0) {
+          ok = mbar_wait(&ms.v_empty[vs], ((jk / NV) & 1) ^ 1);
+          if (ok) mbar_arrive_expect_tx(&ms.v_full[vs], TILE_BYTES);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        for (int i = 0; i < nbox; ++i) {
+          const int r = __shfl_sync(0xffffffffu, row, i);
+          if (lane == 0) {
+            uint8_t* dst = vbuf + vs * TILE_BYTES + i * R * 128;
+            tma_load_3d_hint(dst, &vmap, &ms.v_full[vs], 0, ui.hk, r, policy);
+            tma_load_3d_hint(dst + TT * 128, &vmap, &ms.v_full[vs], 64, ui.hk, r, policy);
+          }
+        }
+        row = nrow;
+        bad = nbad;
+      }
+      ++un;
+    }
+    if (!ok && lane == 0) {
+      set_abort(ms, a.status);
+      // Let armed loads land before the CTA can exit.
+      for (uint32_t j = (jk >= (uint32_t)NK ? jk - NK : 0); j < jk; ++j)
+        mbar_wait(&ms.k_full[j % NK], (j / NK) & 1, 100000000ull);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(128, NPAD, BF16, false, false);
+      const uint32_t id_o = idesc_f16(128, NPAD, BF16, true, false);
+      const uint32_t kaddr = smem_u32(kbuf), vaddr = smem_u32(vbuf);
+      const uint32_t qaddr = smem_u32(qbuf), paddr = smem_u32(pbuf);
+      uint32_t j = 0, un = 0;
+      int prev = -1;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t jp) {
+        const int vs = jp % NV, b = jp & 1;
+        ok = ok && mbar_wait(&ms.v_full[vs], (jp / NV) & 1);
+        ok = ok && mbar_wait(&ms.p_full[b], (jp >> 1) & 1);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t d = tmem + 2 * NPAD + b * NPAD;
+#pragma unroll
+        for (int k = 0; k < TT / 16; ++k) {
+          const uint64_t ad = smem_desc(vaddr + vs * TILE_BYTES + k * 2048, TT * 128, 1024,
+                                        kSwizzle128B);
+          const uint64_t bd = smem_desc(paddr + b * LY::QB + (k >> 2) * NPAD * 128 + (k & 3) * 32,
+                                        16, 1024, kSwizzle128B);
+          mma_f16(d, ad, bd, id_o, k > 0);
+        }
+        mma_commit(&ms.o_full[b]);
+        mma_commit(&ms.v_empty[vs]);
+      };
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const UnitInfo ui = unit_info(a, u);
+        if (ui.ntiles == 0) continue;
+        const int qb = un & 1;
+        ok = mbar_wait(&ms.q_full[qb], (un >> 1) & 1);
+        for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++j) {
+          const int ks = j % NK, b = j & 1;
+          ok = mbar_wait(&ms.k_full[ks], (j / NK) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem + b * NPAD;
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint64_t ad = smem_desc(kaddr + ks * TILE_BYTES + (k >> 2) * TT * 128 + (k & 3) * 32,
+                                          16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(qaddr + qb * LY::QB + (k >> 2) * NPAD * 128 + (k & 3) * 32,
+                                          16, 1024, kSwizzle128B);
+            mma_f16(d, ad, bd, id_s, k > 0);
+          }
+          mma_commit(&ms.s_full[b]);
+          mma_commit(&ms.k_empty[ks]);
+          if (jl == ui.ntiles - 1) mma_commit(&ms.q_empty[qb]);
+          if (prev >= 0) issue_pv((uint32_t)prev);
+          prev = (int)j;
+        }
+        ++un;
+      }
+      if (ok && prev >= 0) issue_pv((uint32_t)prev);
+      if (!ok) set_abort(ms, a.status);
+      // Drain: every MMA issued above has completed once this arrives.
+      mma_commit(&ms.drain);
+      mbar_wait(&ms.drain, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ softmax / epilogue
+    const int wq = warp & 3;                   // TMEM lane quadrant of this warp
+    const int row = wq * 32 + lane;            // token row of S, d row of O
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const float qscale = a.scale * kLog2e;
+    const bool single = a.num_partitions == 1;
+    const int H = a.num_heads;
+    float o_acc[NPAD], l_part[NPAD];
+#pragma unroll
+    for (int h = 0; h < NPAD; ++h) o_acc[h] = l_part[h] = 0.f;
+    uint32_t j = 0;
+    bool ok = true;
+
+    auto accumulate_o = [&](uint32_t jo) {
+      const int b = jo & 1;
+      ok = ok && mbar_wait(&ms.o_full[b], (jo >> 1) & 1);
+      if (!ok) return;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < NPAD / 16; ++c) {
+        float v[16];
+        tmem_ld16(lane_addr + 2 * NPAD + b * NPAD + c * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = c * 16 + i;
+          o_acc[h] = fmaf(o_acc[h], ms.alpha[b][h], v[i]);
+        }
+      }
+      tc_fence_before();
+    };
+
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const UnitInfo ui = unit_info(a, u);
+      const int h0 = ui.hk * g;
+      if (ui.ntiles == 0) {
+        if (single) {
+          uint16_t* o = reinterpret_cast<uint16_t*>(a.out);
+          for (int h = 0; h < g; ++h) o[((size_t)ui.s * H + h0 + h) * HD + row] = 0;
+        }
+        if (!ui.lok && ui.p == 0 && ui.hk == 0 && row == 0) flag(a.status, PKD_DEV_BAD_LEN);
+        continue;
+      }
+      bool unit_bad = false;
+      // Every wait below is bounded; a thread that gives up keeps taking part
+      // in the group barriers, which AND the flag so the group stops together.
+      for (int jl = 0; jl < ui.ntiles; ++jl, ++j) {
+        const int b = j & 1, ks = j % NK, vs = j % NV;
+        const int ts = ui.t0 + jl * TT;
+        const bool valid = ts + row < ui.t1;
+        ok = ok && mbar_wait(&ms.s_full[b], (j >> 1) & 1);
+        ok = ok && mbar_wait(&ms.k_full[ks], (j / NK) & 1);
+        tc_fence_after();
+        unit_bad |= ms.k_bad[ks] != 0;
+        mbar_arrive(&ms.k_empty[ks]);
+        // Tile maxima per head.
+        const uint32_t s_addr = lane_addr + b * NPAD;
+#pragma unroll
+        for (int c = 0; c < NPAD / 16; ++c) {
+          float x[16];
+          tmem_ld16(s_addr + c * 16, x);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (c * 16 + i < g) {
+              const float m = warp_max(valid ? x[i] * qscale : -INFINITY);
+              if (lane == i) ms.red[b][wq][c * 16 + i] = m;
+            }
+          }
+        }
+        ok = named_barrier_and(kSoftmaxBar, kSoftmaxThreads, ok);
+        if (!ok) break;
+        const int et = threadIdx.x - 64;
+        if (et < g) {
+          const float mt = fmaxf(fmaxf(ms.red[b][0][et], ms.red[b][1][et]),
+                                 fmaxf(ms.red[b][2][et], ms.red[b][3][et]));
+          const float m_old = ms.m_run[et];
+          const float m_new = fmaxf(m_old, mt);
+          ms.alpha[b][et] = m_new == -INFINITY ? 1.f : exp2f(m_old - m_new);
+          ms.m_run[et] = m_new;
+        }
+        named_barrier(kSoftmaxBar, kSoftmaxThreads);
+        // Probabilities: written 16-bit into the P^T operand, summed per thread.
+        uint8_t* pb = pbuf + b * LY::QB;
+#pragma unroll
+        for (int c = 0; c < NPAD / 16; ++c) {
+          float x[16];
+          tmem_ld16(s_addr + c * 16, x);
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const int h = c * 16 + i;
+            float p0 = 0.f, p1 = 0.f;
+            if (h < g) {
+              p0 = valid ? exp2f(x[i] * qscale - ms.m_run[h]) : 0.f;
+              l_part[h] = fmaf(l_part[h], ms.alpha[b][h], p0);
+            }
+            if (h + 1 < g) {
+              p1 = valid ? exp2f(x[i + 1] * qscale - ms.m_run[h + 1]) : 0.f;
+              l_part[h + 1] = fmaf(l_part[h + 1], ms.alpha[b][h + 1], p1);
+            }
+            const uint32_t pk = pack2<BF16>(p0, p1);
+            if (h < g) *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row, NPAD)) = (uint16_t)pk;
+            if (h + 1 < g)
+              *reinterpret_cast<uint16_t*>(pb + sw128_offset(h + 1, row, NPAD)) = (uint16_t)(pk >> 16);
+          }
+        }
+        // Cache slots past the sequence end inside a loaded block may hold
+        // anything (NaN included): zero those V rows before P V reads them.
+        if (ts + TT > ui.L) {
+          ok = ok && mbar_wait(&ms.v_full[vs], (j / NV) & 1);
+          if (ok && ts + row >= ui.L) {
+            uint4* v0 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + row * 128);
+            uint4* v1 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + TT * 128 + row * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&ms.p_full[b]);
+        if (jl > 0) accumulate_o(j - 1);
+        if (jl == ui.ntiles - 1) accumulate_o(j);
+      }
+      // ---------------------------------------------------------- finalise unit
+#pragma unroll
+      for (int h = 0; h < NPAD; ++h) {
+        if (h < g) {
+          const float t = warp_sum(l_part[h]);
+          if (lane == 0) ms.lsum[wq][h] = t;
+        }
+      }
+      ok = named_barrier_and(kSoftmaxBar, kSoftmaxThreads, ok);
+      if (!ok) break;
+      const size_t sp0 = (size_t)ui.s * H + h0;
+      if (single) {
+        uint16_t* o = reinterpret_cast<uint16_t*>(a.out);
+#pragma unroll
+        for (int h = 0; h < NPAD; ++h) {
+          if (h < g) {
+            const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
+            const float v = unit_bad ? 0.f : o_acc[h] / den;
+            o[(sp0 + h) * HD + row] = (uint16_t)pack2<BF16>(v, 0.f);
+          }
+        }
+      } else {
+        const int P = a.num_partitions;
+#pragma unroll
+        for (int h = 0; h < NPAD; ++h) {
+          if (h < g) a.ws_o[((sp0 + h) * P + ui.p) * HD + row] = o_acc[h];
+        }
+        const int et = threadIdx.x - 64;
+        if (et < g) {
+          const float den = ms.lsum[0][et] + ms.lsum[1][et] + ms.lsum[2][et] + ms.lsum[3][et];
+          a.ws_m[(sp0 + et) * P + ui.p] = ms.m_run[et];
+          a.ws_l[(sp0 + et) * P + ui.p] = unit_bad ? -1.f : den;
+        }
+      }
+      named_barrier(kSoftmaxBar, kSoftmaxThreads);
+      const int et = threadIdx.x - 64;
+      if (et < 64) ms.m_run[et] = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < NPAD; ++h) o_acc[h] = l_part[h] = 0.f;
+    }
+    if (!ok && threadIdx.x == 64) set_abort(ms, a.status);
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols(NPAD));
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+int pad_group(int g) { return (g + 15) / 16 * 16; }
+
+template <bool BF16, int NPAD>
+cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUtensorMap km, vm, qm;
+  const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)a.num_kv_heads,
+                              (cuuint64_t)a.num_blocks * a.block_size};
+  const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)a.num_kv_heads * HD * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)(a.block_size < TT ? a.block_size : TT)};
+  if (enc(&km, dt, 3, const_cast<void*>(a.key_cache), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&vm, dt, 3, const_cast<void*>(a.value_cache), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const cuuint64_t qdims[2] = {(cuuint64_t)HD, (cuuint64_t)a.num_seqs * a.num_heads};
+  const cuuint64_t qstrides[1] = {(cuuint64_t)HD * 2};
+  const cuuint32_t qbox[2] = {64, (cuuint32_t)NPAD};
+  if (enc(&qm, dt, 2, const_cast<void*>(a.q), qdims, qstrides, qbox, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  const int smem = SmemLayout<NPAD>::bytes + 1024;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  const int grid = (int)(units < sms ? units : sms);
+  decode_tc_kernel<BF16, NPAD><<<grid, kThreads, smem, st>>>(km, vm, qm, a);
+  return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_b(const DecodeArgs& a, cudaStream_t st) {
+  switch (pad_group(a.num_heads / a.num_kv_heads)) {
+    case 16: return launch_t<BF16, 16>(a, st);
+    case 32: return launch_t<BF16, 32>(a, st);
+    case 48: return launch_t<BF16, 48>(a, st);
+    case 64: return launch_t<BF16, 64>(a, st);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+bool decode_tc_supported(int head_size, int group, int block_size) {
+  return head_size == HD && group >= 4 && group <= 64 && block_size >= 8 && encode_fn() != nullptr;
+}
+
+int decode_tc_tile() { return TT; }
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
+  return a.is_bf16 ? launch_b<true>(a, st) : launch_b<false>(a, st);
+}
 
 }  // namespace pkd

@@ -51,6 +51,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 int simt_heads_per_cta(int group);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 bool decode_tc_supported(int head_size, int group, int block_size);
+int decode_tc_tile();
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st);

@@ -74,6 +74,7 @@ RAGGED = [
     (8, 8, 128, 16, "fp16"), (8, 4, 128, 8, "bf16"), (12, 4, 64, 32, "fp16"),
     (16, 4, 128, 64, "bf16"), (64, 8, 128, 16, "bf16"), (48, 1, 128, 16, "fp16"),
     (16, 2, 64, 128, "bf16"), (8, 1, 128, 256, "fp16"), (4, 4, 64, 16, "bf16"),
+    (32, 1, 128, 16, "bf16"), (64, 1, 128, 32, "fp16"), (40, 8, 128, 16, "bf16"),
 ]
 
 
