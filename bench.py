@@ -215,6 +215,78 @@ def cpu_baseline(c, g, budget_s=10.0):
             "kind": "oracle", "sample": f"{what}; {n} passes in {el:.1f} s"}
 
 
+def device_decode_inputs(name, dev):
+    """Device inputs of a decode workload from a seeded torch generator (for
+    timing and profiling: the kernels' speed does not depend on the values)."""
+    import torch
+
+    from paged_kv_decode_22_gb300.workloads import decode_configs
+    cfg = decode_configs()[name]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg["seed"])
+    S, H, Hk, D, B = (cfg["num_seqs"], cfg["num_heads"], cfg["num_kv_heads"], cfg["head_size"],
+                      cfg["block_size"])
+    lens = torch.tensor(cfg["context_lens"], dtype=torch.int32)
+    need = (lens + B - 1) // B
+    nb = max(cfg["num_blocks"], int(need.sum()))
+    dt = torch.float16 if cfg["dtype"] == "fp16" else torch.bfloat16
+    kc = torch.randn((nb, B, Hk, D), generator=gen, device=dev, dtype=dt)
+    vc = torch.randn((nb, B, Hk, D), generator=gen, device=dev, dtype=dt)
+    q = torch.randn((S, H, D), generator=gen, device=dev, dtype=dt)
+    perm = torch.randperm(nb, generator=gen, device=dev).to(torch.int32)
+    mb = int(need.max())
+    bt = torch.zeros((S, mb), dtype=torch.int32, device=dev)
+    pos = 0
+    for s in range(S):
+        n = int(need[s])
+        bt[s, :n] = perm[pos:pos + n]
+        pos += n
+    nbytes = (int(lens.sum()) * Hk * D * 2 * 2 + 2 * S * H * D * 2 + 4 * int(need.sum()) + 4 * S)
+    return dict(q=q, kc=kc, vc=vc, bt=bt, cl=lens.to(dev), max_ctx=int(lens.max()),
+                scale=1.0 / math.sqrt(D), out=torch.empty_like(q), bytes=nbytes)
+
+
+def run_profile(args, local):
+    """Run one kernel family on one workload (no timing): the command ncu wraps."""
+    import torch
+
+    from paged_kv_decode_22_gb300 import ops
+    from paged_kv_decode_22_gb300.workloads import gather_sweep, make_gather_case
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kind, name = args.profile.split(":", 1)
+    if kind == "decode":
+        d = device_decode_inputs(name, dev)
+        S, H, D = d["q"].shape
+        _, npart, _, ws = ops.decode_plan(S, H, d["kc"].shape[2], D, d["kc"].shape[1],
+                                          d["max_ctx"])
+        work = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+
+        def call():
+            ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"], d["cl"],
+                                       d["max_ctx"], d["scale"], workspace=work)
+    elif kind == "gather":
+        g = make_gather_case(name=name, **gather_sweep()[name])
+        import numpy as np
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.float16).to(dev)
+        kc, vc = up(g.key_cache), up(g.value_cache)
+        slots = torch.from_numpy(g.slot_mapping).to(dev)
+        ko = torch.empty((g.num_tokens, g.num_heads, g.head_size), dtype=torch.float16,
+                         device=dev)
+        vo = torch.empty_like(ko)
+
+        def call():
+            ops.gather_cached_kv(ko, vo, kc, vc, slots)
+    else:
+        raise SystemExit(f"unknown profile kind {kind}")
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    print(f"profile {args.profile}: {args.warmup + args.steps} calls ok")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -223,6 +295,9 @@ def main():
     ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
     ap.add_argument("--no-targets", action="store_true", help="skip the large-batch GQA lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--profile", default=None, metavar="KIND:NAME",
+                    help="profiling mode: run only 'decode:<workload>' or 'gather:<workload>' "
+                         "warmup + steps times (no timing, no JSON line), e.g. under ncu")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -232,6 +307,8 @@ def main():
     if args.impl == "reference":
         # Only rank 0 times the oracle; other ranks exit without work.
         return run_reference(args, world, rank)
+    if args.profile:
+        return run_profile(args, local)
     import numpy as np
     import torch
 

@@ -11,11 +11,13 @@
 // one CTA per SM walks its units round-robin; inside the CTA, warps are
 // specialised and linked by mbarriers so the K/V stream never stops at unit
 // boundaries:
-//   warp 0     producer: reads block ids, issues TMA loads of q (per unit)
-//              and of K and V tiles (128 tokens) into rings of 32 KB stages.
-//              Blocks past the partition end (and out-of-range ids) are
-//              loaded from an out-of-bounds coordinate, which TMA fills with
-//              zeros without touching memory.
+//   warps 0, 6 producers (K and q; V): read block ids one tile ahead and
+//              issue the TMA loads of a 128-token tile from up to 32 lanes
+//              at once (one box per block and 64-column half) into rings of
+//              32 KB stages.  Blocks past the partition end (and
+//              out-of-range ids) are loaded from an out-of-bounds
+//              coordinate, which TMA fills with zeros without touching
+//              memory.
 //   warp 1     MMA issuer (one thread): S^T = K q^T (M = 128 tokens,
 //              N = group padded to 16) into TMEM, then O^T = V^T P^T
 //              (M = 128 = head_size, K = 128 tokens).
@@ -40,8 +42,10 @@ using namespace sm100;
 constexpr int TT = 128;                 // tokens per tile (= MMA M for S)
 constexpr int HD = 128;                 // head_size of this path (= MMA M for O)
 constexpr int TILE_BYTES = TT * HD * 2; // one K or V tile, 32 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;          // 7 warps, roles below
+constexpr int kVWarp = 6;              // V producer (warp 0 produces K and q)
 constexpr int kSoftmaxThreads = 128;
+constexpr int kNoBlock = -2147483647 - 1;  // "no block here" marker of the producers
 constexpr uint32_t kSoftmaxBar = 1;     // named barrier id of warps 2-5
 
 __host__ __device__ constexpr int k_stages(int npad) { return npad <= 48 ? 3 : 2; }
@@ -70,9 +74,9 @@ struct Misc {
   uint32_t tmem_base;
   int abort;
   int k_bad[3];                 // per K stage: the tile referenced a bad block id
-  float red[2][4][64];          // per-warp tile maxima
-  float m_run[64];              // running maxima (log2 domain)
-  float alpha[2][64];           // rescale factor of each tile parity
+  alignas(16) float red[2][4][64];   // per-warp tile maxima
+  alignas(16) float m_run[64];       // running maxima (log2 domain)
+  alignas(16) float alpha[2][64];    // rescale factor of each tile parity
   float lsum[4][64];            // per-warp exponent sums at finalisation
 };
 
@@ -113,6 +117,25 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// Maximum over the 32 lanes of each of 16 per-lane values, by a butterfly
+// that halves the values each step (16 shuffles instead of 80).  Lane l ends
+// with the result for value (l >> 1) & 15.
+__device__ __forceinline__ float warp_max16(const float (&v)[16], int lane) {
+  float w8[8], w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w8[i] = fmaxf(b4 ? v[8 + i] : v[i], __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[8 + i], 16));
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w4[i] = fmaxf(b3 ? w8[4 + i] : w8[i], __shfl_xor_sync(0xffffffffu, b3 ? w8[i] : w8[4 + i], 8));
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    w2[i] = fmaxf(b2 ? w4[2 + i] : w4[i], __shfl_xor_sync(0xffffffffu, b2 ? w4[i] : w4[2 + i], 4));
+  float w1 = fmaxf(b1 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2));
+  return fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -180,20 +203,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
 
-  if (warp == 0) {
-    // ============================================================ producer
+  if (warp == 0 || warp == kVWarp) {
+    // ============================================================ producers
+    const bool is_v = warp == kVWarp;
     const int B = a.block_size;
     const int R = B < TT ? B : TT;            // rows per TMA box
     const int nbox = TT / R;                  // boxes per tile and 64-column half
     const int oob_row = a.num_blocks * B;     // first row past the pool: zero fill
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    uint8_t* ring = is_v ? vbuf : kbuf;
+    const int nst = is_v ? NV : NK;
+    uint64_t* full = is_v ? ms.v_full : ms.k_full;
+    uint64_t* empty = is_v ? ms.v_empty : ms.k_empty;
     const uint64_t policy = policy_evict_first();
+    const bool issuer = lane < 2 * nbox;      // lane issues box (lane % nbox) of half (lane / nbox)
+    const int my_box = lane % nbox, my_half = lane / nbox;
+
+    auto next_unit = [&](int from, UnitInfo& out) {
+      for (int x = from; x < n_units; x += gridDim.x) {
+        out = unit_info(a, x);
+        if (out.ntiles) return x;
+      }
+      return n_units;
+    };
+    // Raw block id of box `lane` of tile tj (lanes < nbox), kNoBlock if the
+    // box lies past the partition end.  The loaded value is first used one
+    // tile later, so its latency hides behind the current tile's issue.
+    auto load_raw = [&](const UnitInfo& t, int tj) {
+      int raw = kNoBlock;
+      if (lane < nbox) {
+        const int ts = t.t0 + tj * TT;
+        const int tok0 = B <= TT ? ts + lane * B : ts;
+        if (tok0 < t.t1) raw = __ldg(a.block_tables + (size_t)t.s * a.max_blocks_per_seq + tok0 / B);
+      }
+      return raw;
+    };
+    UnitInfo ui;
+    int u = next_unit(blockIdx.x, ui), jl = 0;
+    int raw = u < n_units ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const UnitInfo ui = unit_info(a, u);
-      if (ui.ntiles == 0) continue;
-      const int32_t* bt = a.block_tables + (size_t)ui.s * a.max_blocks_per_seq;
-      if (lane == 0) {
+    while (u < n_units) {
+      UnitInfo nui = ui;
+      int nu = u, njl = jl + 1;
+      if (njl >= ui.ntiles) {
+        nu = next_unit(u + gridDim.x, nui);
+        njl = 0;
+      }
+      const int nraw = nu < n_units ? load_raw(nui, njl) : kNoBlock;
+      if (!is_v && jl == 0 && lane == 0) {
         const int qb = un & 1;
         ok = mbar_wait(&ms.q_empty[qb], ((un >> 1) & 1) ^ 1);
         if (ok) {
@@ -203,72 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, row0);
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      // Block ids of the first tile; later tiles are fetched one tile ahead.
-      auto fetch = [&](int jl, int& row, bool& bad) {
-        const int ts = ui.t0 + jl * TT;
-        row = oob_row;
-        bad = false;
-        if (lane < nbox) {
-          const int tok0 = B <= TT ? ts + lane * B : ts;
-          if (tok0 < ui.t1) {
-            const int id = __ldg(bt + tok0 / B);
-            if (id >= 0 && id < a.num_blocks)
-              row = id * B + (B <= TT ? 0 : (ts % B));
-            else
-              bad = true;
+      const int ts = ui.t0 + jl * TT;
+      const bool bad = raw != kNoBlock && (raw < 0 || raw >= a.num_blocks);
+      const int row = (raw != kNoBlock && !bad) ? raw * B + (B <= TT ? 0 : ts % B) : oob_row;
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      const int st = jk % nst;
+      if (lane == 0) {
+        ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
+        if (ok) {
+          if (!is_v) {
+            ms.k_bad[st] = any_bad ? 1 : 0;
+            if (any_bad) flag(a.status, PKD_DEV_BAD_BLOCK);
           }
+          mbar_arrive_expect_tx(&full[st], TILE_BYTES);
         }
-      };
-      int row, nrow;
-      bool bad, nbad;
-      fetch(0, row, bad);
-      for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++jk) {
-        if (jl + 1 < ui.ntiles) fetch(jl + 1, nrow, nbad);
-        const bool any_bad = __any_sync(0xffffffffu, bad);
-        if (any_bad && lane == 0) flag(a.status, PKD_DEV_BAD_BLOCK);
-        const int ks = jk % NK, vs = jk % NV;
-        if (lane == 0) {
-          ok = mbar_wait(&ms.k_empty[ks], ((jk / NK) & 1) ^ 1);
-          if (ok) {
-            ms.k_bad[ks] = any_bad ? 1 : 0;
-            mbar_arrive_expect_tx(&ms.k_full[ks], TILE_BYTES);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        for (int i = 0; i < nbox; ++i) {
-          const int r = __shfl_sync(0xffffffffu, row, i);
-          if (lane == 0) {
-            uint8_t* dst = kbuf + ks * TILE_BYTES + i * R * 128;
-            tma_load_3d_hint(dst, &kmap, &ms.k_full[ks], 0, ui.hk, r, policy);
-            tma_load_3d_hint(dst + TT * 128, &kmap, &ms.k_full[ks], 64, ui.hk, r, policy);
-          }
-        }
-        if (lane == 0) {
-          ok = mbar_wait(&ms.v_empty[vs], ((jk / NV) & 1) ^ 1);
-          if (ok) mbar_arrive_expect_tx(&ms.v_full[vs], TILE_BYTES);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        for (int i = 0; i < nbox; ++i) {
-          const int r = __shfl_sync(0xffffffffu, row, i);
-          if (lane == 0) {
-            uint8_t* dst = vbuf + vs * TILE_BYTES + i * R * 128;
-            tma_load_3d_hint(dst, &vmap, &ms.v_full[vs], 0, ui.hk, r, policy);
-            tma_load_3d_hint(dst + TT * 128, &vmap, &ms.v_full[vs], 64, ui.hk, r, policy);
-          }
-        }
-        row = nrow;
-        bad = nbad;
       }
-      ++un;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int r = __shfl_sync(0xffffffffu, row, my_box);
+      if (issuer)
+        tma_load_3d_hint(ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128, map,
+                         &full[st], my_half * 64, ui.hk, r, policy);
+      ++jk;
+      if (nu != u) ++un;
+      u = nu;
+      ui = nui;
+      jl = njl;
+      raw = nraw;
     }
     if (!ok && lane == 0) {
       set_abort(ms, a.status);
       // Let armed loads land before the CTA can exit.
-      for (uint32_t j = (jk >= (uint32_t)NK ? jk - NK : 0); j < jk; ++j)
-        mbar_wait(&ms.k_full[j % NK], (j / NK) & 1, 100000000ull);
+      for (uint32_t j = (jk >= (uint32_t)nst ? jk - nst : 0); j < jk; ++j)
+        mbar_wait(&full[j % nst], (j / nst) & 1, 100000000ull);
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
@@ -387,19 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         unit_bad |= ms.k_bad[ks] != 0;
         mbar_arrive(&ms.k_empty[ks]);
-        // Tile maxima per head.
+        // Tile maxima per head (logits kept in registers for the exponentials).
         const uint32_t s_addr = lane_addr + b * NPAD;
+        float xs[NPAD];
 #pragma unroll
         for (int c = 0; c < NPAD / 16; ++c) {
           float x[16];
           tmem_ld16(s_addr + c * 16, x);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            if (c * 16 + i < g) {
-              const float m = warp_max(valid ? x[i] * qscale : -INFINITY);
-              if (lane == i) ms.red[b][wq][c * 16 + i] = m;
-            }
+            x[i] = valid ? x[i] * qscale : -INFINITY;
+            xs[c * 16 + i] = x[i];
           }
+          const float m = warp_max16(x, lane);
+          if ((lane & 1) == 0) ms.red[b][wq][c * 16 + (lane >> 1)] = m;
         }
         ok = named_barrier_and(kSoftmaxBar, kSoftmaxThreads, ok);
         if (!ok) break;
@@ -417,20 +443,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* pb = pbuf + b * LY::QB;
 #pragma unroll
         for (int c = 0; c < NPAD / 16; ++c) {
-          float x[16];
-          tmem_ld16(s_addr + c * 16, x);
+          float mr[16], al[16];
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            *reinterpret_cast<float4*>(&mr[i]) = *reinterpret_cast<const float4*>(&ms.m_run[c * 16 + i]);
+            *reinterpret_cast<float4*>(&al[i]) = *reinterpret_cast<const float4*>(&ms.alpha[b][c * 16 + i]);
+          }
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             const int h = c * 16 + i;
-            float p0 = 0.f, p1 = 0.f;
-            if (h < g) {
-              p0 = valid ? exp2f(x[i] * qscale - ms.m_run[h]) : 0.f;
-              l_part[h] = fmaf(l_part[h], ms.alpha[b][h], p0);
-            }
-            if (h + 1 < g) {
-              p1 = valid ? exp2f(x[i + 1] * qscale - ms.m_run[h + 1]) : 0.f;
-              l_part[h + 1] = fmaf(l_part[h + 1], ms.alpha[b][h + 1], p1);
-            }
+            const float p0 = (valid && h < g) ? exp2f(xs[h] - mr[i]) : 0.f;
+            const float p1 = (valid && h + 1 < g) ? exp2f(xs[h + 1] - mr[i + 1]) : 0.f;
+            l_part[h] = fmaf(l_part[h], al[i], p0);
+            l_part[h + 1] = fmaf(l_part[h + 1], al[i + 1], p1);
             const uint32_t pk = pack2<BF16>(p0, p1);
             if (h < g) *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row, NPAD)) = (uint16_t)pk;
             if (h + 1 < g)
