@@ -131,6 +131,41 @@ PKD_API pkd_status pkd_paged_decode_attention(void* out, const void* q, const vo
                                       size_t workspace_bytes, uint32_t* device_status,
                                       void* stream);
 
+/* Size of the scratch array built into the library for
+ * pkd_paged_decode_attention_static_ws (16 MiB per GPU that loads it). */
+#define PKD_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+
+/*
+ * Decode attention for callers that cannot allocate device memory.  (The
+ * vLLM pages have no counterpart: this is an interface addition.)
+ *
+ * Same arguments, results and errors as pkd_paged_decode_attention, minus
+ * the workspace: the split-context scratch comes from an array of
+ * PKD_STATIC_WORKSPACE_BYTES bytes compiled into the library, so the call
+ * allocates nothing and needs nothing from the caller beyond inputs and
+ * outputs.  It serves code that must not call cudaMalloc while it runs -- a
+ * serving loop that may never touch the allocator, a runtime whose device
+ * memory is pre-carved by another owner, an operator plugin handed only its
+ * input and output pointers.
+ *   - Returns PKD_ERR_WORKSPACE, launching nothing, when the launch plan
+ *     (pkd_decode_plan with the same sizes) needs more scratch than
+ *     PKD_STATIC_WORKSPACE_BYTES; pass a larger partition_size, or use
+ *     pkd_paged_decode_attention with a caller-provided workspace.
+ *   - The first call on each device, with that device current, looks up the
+ *     array's device address once (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; nothing in it needs to start at zero.  Calls that
+ *     overlap on the GPU (e.g. on two streams at once) race on it: order them.
+ *   - Every GPU that loads the library holds the array until process exit.
+ */
+PKD_API pkd_status pkd_paged_decode_attention_static_ws(
+    void* out, const void* q, const void* key_cache, const void* value_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int num_blocks, float scale, pkd_dtype dtype, int partition_size,
+    uint32_t* device_status, void* stream);
+
 /*
  * gather_cached_kv: key_out[t] = key_cache[slot / block_size][slot % block_size]
  * and value_out[t] likewise, slot = slot_mapping[t], bit for bit.

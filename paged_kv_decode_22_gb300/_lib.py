@@ -28,6 +28,8 @@ _SIGS = {
                         [ctypes.POINTER(_c_size)]),
     "pkd_paged_decode_attention": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
                                    [_c_float, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
+    "pkd_paged_decode_attention_static_ws": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
+                                             [_c_float, _c_int, _c_int, _vp, _vp]),
     "pkd_gather_cached_kv": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_vp, _vp]),
     "pkd_reshape_and_cache": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_vp, _vp]),
     "pkd_status_string": (ctypes.c_char_p, [_c_int]),
@@ -132,6 +134,25 @@ def paged_decode_attention(out, q, key_cache, value_cache, block_tables, context
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(device_status), _stream(stream))
     _check("pkd_paged_decode_attention", st)
+    return out
+
+
+def paged_decode_attention_static_ws(out, q, key_cache, value_cache, block_tables, context_lens,
+                                     max_context_len, scale, partition_size=0,
+                                     device_status=None, stream=None):
+    """paged_decode_attention without a workspace argument, for callers that
+    cannot allocate device memory: the library's built-in scratch array is
+    used (see pkd_paged_decode_attention_static_ws in include/pkd.h)."""
+    _dense(out, q, key_cache, value_cache, block_tables, context_lens, device_status)
+    S, H, D = q.shape
+    NB, B, Hk, _ = key_cache.shape
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    st = lib().pkd_paged_decode_attention_static_ws(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), max_context_len, S, H, Hk, D, B, NB,
+        float(scale), _dtype_code(q), partition_size, _ptr(device_status), _stream(stream))
+    _check("pkd_paged_decode_attention_static_ws", st)
     return out
 
 
