@@ -105,7 +105,9 @@ PKD_API pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads
  *   key_cache,
  *   value_cache   [num_blocks][block_size][num_kv_heads][head_size] 16-bit
  *   block_tables  [num_seqs][max_blocks_per_seq] int32; entries past
- *                 ceil(context_lens[s] / block_size) are never read
+ *                 ceil(context_lens[s] / block_size) are ignored (their
+ *                 values do not matter; max_blocks_per_seq * block_size
+ *                 must stay below 2^31 - 2^16)
  *   context_lens  [num_seqs] int32, each in [0, max_context_len]
  *   max_context_len  host-side upper bound of context_lens (sizes the grid)
  *   num_heads % num_kv_heads == 0;  head_size in {64, 128};

@@ -51,7 +51,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
 
 constexpr int kPartitionQuantum = 64;   // partitions are whole 64-token tiles
-constexpr int kTargetCtasPerSm = 4;     // split until about this many CTAs per SM
+constexpr int kTargetCtasPerSm = 2;     // split until about this many CTAs per SM
 
 struct Plan {
   int partition_size = kPartitionQuantum;
@@ -169,6 +169,7 @@ pkd_status pkd_paged_decode_attention(void* out, const void* q, const void* key_
   if (!pow2_in(block_size, 8, 256)) return PKD_ERR_UNSUPPORTED;
   if (num_blocks < 1 || max_blocks_per_seq < 1) return PKD_ERR_SHAPE;
   if ((long long)num_blocks * block_size > 0x7fffffffLL) return PKD_ERR_SHAPE;
+  if ((long long)max_blocks_per_seq * block_size > 0x7fff0000LL) return PKD_ERR_SHAPE;
   if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
     return PKD_ERR_ALIGN;
   Plan plan;

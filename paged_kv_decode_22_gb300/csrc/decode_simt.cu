@@ -1,6 +1,6 @@
 // Decode attention over a paged KV cache on the CUDA cores (query-group
-// sizes below 4, and head_size / block_size combinations the tensor-core
-// path does not take).
+// sizes below 4, head_size 64, and partitions the tensor-core path does not
+// take).
 //
 // One CTA of 4 warps handles one (sequence, KV head, head chunk, context
 // partition).  It computes, for the GC query heads of the chunk,
@@ -11,35 +11,67 @@
 // registers, so no thread group re-reads it per token (the point of
 // "Optimizes the single_query_cached_kv_attention kernel", pull request 420).
 //
+// Latency: the context length, the partition's block ids (into shared
+// memory) and the query are requested together at entry, so only one global
+// round trip precedes the first K/V load.  Table entries of the partition past
+// the sequence end are read with the others but never used.  K and V reach
+// shared memory by TMA: each warp owns a ring of 4 stages, one stage being
+// the K and V rows of 8 consecutive tokens of one block (two boxes, 4 KB at
+// head_size 128), so a warp keeps up to 16 KB of loads in flight while it
+// computes, with two TMA instructions per 8 tokens.  Rows a box brings in
+// past the partition end or the sequence end are masked (their V is read as
+// zero: cache slots past the end may hold anything, NaN included); boxes of
+// out-of-range block ids read an out-of-bounds row, which TMA fills with zeros.
+//
 // Lane layout: D/8 lanes share one token row, each holding 8 consecutive
 // elements (one 16-byte load of K and one of V per token), so a warp row
 // covers 32/(D/8) tokens with fully coalesced 256-byte (D=128) rows.  Each
 // warp runs its own online softmax over the tokens it loads; the four warps
-// are merged through shared memory at the end.  Block ids are fetched one
-// iteration ahead so the id load never sits in front of the K/V loads.
+// are merged through shared memory at the end.
 //
 // Output: with one partition the CTA writes `out` directly; otherwise it
 // writes the unnormalised partial (o, m, l) that lse_reduce.cu merges.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace pkd {
 namespace {
 
+using namespace sm100;
+
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kUnroll = 4;
+constexpr int kRows = 8;        // tokens per warp iteration = rows of one TMA box
+constexpr int kStages = 4;      // ring depth per warp
+constexpr int kMaxIds = 1024;   // block ids staged in shared memory per pass
+
+template <int D>
+struct Ring {
+  static constexpr int box = kRows * D * 2;           // K (or V) rows of one stage
+  static constexpr int stage = 2 * box;
+  static constexpr int bytes = kWarps * kStages * stage + 128;   // + alignment slack
+};
 
 template <bool BF16, int D, int GC>
-__global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads)
+    decode_simt_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   constexpr int TPG = D / 8;       // lanes per token row
   constexpr int SUBS = 32 / TPG;   // token rows per warp row
-  constexpr int WT = SUBS * kUnroll;
-  constexpr int CT = kWarps * WT;  // tokens per CTA iteration
+  constexpr int U = kRows / SUBS;  // rows per lane per iteration
+  static_assert(U * SUBS == kRows, "one box per warp iteration");
+  extern __shared__ __align__(128) uint8_t ring_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) &
+                                             ~uintptr_t(127));
+  __shared__ uint64_t full[kWarps][kStages];
 
   __shared__ float red_m[kWarps][GC];
   __shared__ float red_l[kWarps][GC];
   __shared__ __align__(16) float red_o[kWarps][GC][D];
+  __shared__ int ids[kMaxIds];
 
   const int s = blockIdx.z;
   const int g = a.num_heads / a.num_kv_heads;
@@ -51,11 +83,37 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
   const int sub = lane / TPG, part = lane % TPG;
   const bool single = a.num_partitions == 1;
   const int H = a.num_heads;
+  const int lb = __ffs(a.block_size) - 1;  // block_size is a power of two
+  const int bmask = a.block_size - 1;
+  const int t0 = p * a.partition_size;
+  const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks_per_seq;
 
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w)
+      for (int i = 0; i < kStages; ++i) mbar_init(&full[w][i], 1);
+    fence_barrier_init();
+  }
+  // ---- entry: length, block ids of this partition (first pass) and q together
   const int L = a.context_lens[s];
+  const int tab_tokens = a.max_blocks_per_seq << lb;
+  const int blk_first = t0 >> lb;   // first block of the partition
+  const int blk_end = t0 < tab_tokens ? ((min(t0 + a.partition_size, tab_tokens) - 1) >> lb) + 1 : blk_first;
+  {
+    const int n = min(blk_end - blk_first, kMaxIds);
+    for (int i = threadIdx.x; i < n; i += kThreads) ids[i] = __ldg(bt + blk_first + i);
+  }
+
+  const float qscale = a.scale * kLog2e;
+  uint4 qw[GC];
+  {
+    const uint16_t* qp =
+        reinterpret_cast<const uint16_t*>(a.q) + ((size_t)s * H + h0) * D + part * 8;
+#pragma unroll
+    for (int j = 0; j < GC; ++j) qw[j] = *reinterpret_cast<const uint4*>(qp + (size_t)j * D);
+  }
+
   const bool lok = len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
   if (!lok && p == 0 && blockIdx.y == 0 && threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
-  const int t0 = p * a.partition_size;
   if (!lok || t0 >= L) {
     // Nothing to attend to.  Unsplit: write the zero row here.  Split: the
     // reduction reads context_lens itself and writes zeros.
@@ -67,25 +125,16 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     return;
   }
   const int t1 = min(t0 + a.partition_size, L);
-  const int lb = __ffs(a.block_size) - 1;  // block_size is a power of two
-  const int bmask = a.block_size - 1;
 
-  // Query chunk: 8 elements per lane and head, pre-scaled so exp2 can be used.
-  const float qscale = a.scale * kLog2e;
   float qr[GC][8];
-  {
-    const uint16_t* qp =
-        reinterpret_cast<const uint16_t*>(a.q) + ((size_t)s * H + h0) * D + part * 8;
 #pragma unroll
-    for (int j = 0; j < GC; ++j) {
-      uint4 w = *reinterpret_cast<const uint4*>(qp + (size_t)j * D);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  for (int j = 0; j < GC; ++j) {
+    const uint32_t ww[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 f = unpack2<BF16>(ww[i]);
-        qr[j][2 * i] = f.x * qscale;
-        qr[j][2 * i + 1] = f.y * qscale;
-      }
+    for (int i = 0; i < 4; ++i) {
+      float2 f = unpack2<BF16>(ww[i]);
+      qr[j][2 * i] = f.x * qscale;
+      qr[j][2 * i + 1] = f.y * qscale;
     }
   }
 
@@ -98,67 +147,70 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
   }
 
-  const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks_per_seq;
   const size_t slot_stride = (size_t)a.num_kv_heads * D;  // elements per cache slot
   const uint16_t* kbase = reinterpret_cast<const uint16_t*>(a.key_cache) + (size_t)hk * D + part * 8;
   const uint16_t* vbase = reinterpret_cast<const uint16_t*>(a.value_cache) + (size_t)hk * D + part * 8;
   bool bad = false;
 
-  int ids[kUnroll];
-  int base = t0 + warp * WT;
-#pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int t = base + u * SUBS + sub;
-    ids[u] = t < t1 ? __ldg(bt + (t >> lb)) : 0;
-  }
+  // Blocks [pb0, pb0 + kMaxIds) of the partition have their ids in shared memory.
+  int pb0 = blk_first;
+  __syncthreads();
 
-  for (; base < t1; base += CT) {
-    // Issue this iteration's K/V loads, then prefetch the next iteration's ids.
-    uint4 kr[kUnroll], vr[kUnroll];
-    bool ok[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = base + u * SUBS + sub;
-      const int id = ids[u];
+  uint8_t* wring = ring + warp * kStages * Ring<D>::stage;
+  const int oob_row = a.num_blocks << lb;   // first row past the pool: TMA zero fill
+  uint32_t wi_issue = 0, wi_use = 0;        // this warp's ring counters
+  bool ok_wait = true;
+
+  // Request the K and V rows of tokens [tb, tb + 8) into the next stage.
+  auto issue = [&](int tb) {
+    const int st = wi_issue % kStages;
+    if (lane == 0) {
+      const int id = ids[(tb >> lb) - pb0];
       const bool in_range = id >= 0 && id < a.num_blocks;
-      ok[u] = t < t1 && in_range;
-      bad |= (t < t1) && !in_range;
-      if (ok[u]) {
-        const size_t row = ((size_t)id << lb) + (t & bmask);
-        kr[u] = ld_stream(kbase + row * slot_stride);
-        vr[u] = ld_stream(vbase + row * slot_stride);
-      } else {
-        kr[u] = make_uint4(0, 0, 0, 0);
-        vr[u] = make_uint4(0, 0, 0, 0);
-      }
+      bad |= !in_range;
+      const int row = in_range ? (id << lb) + (tb & bmask) : oob_row;
+      uint8_t* dst = wring + st * Ring<D>::stage;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&full[warp][st], Ring<D>::stage);
+      tma_load_3d(dst, &kmap, &full[warp][st], 0, hk, row);
+      tma_load_3d(dst + Ring<D>::box, &vmap, &full[warp][st], 0, hk, row);
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = base + CT + u * SUBS + sub;
-      ids[u] = t < t1 ? __ldg(bt + (t >> lb)) : 0;
-    }
+    ++wi_issue;
+  };
 
-    float kf[kUnroll][8], vf[kUnroll][8];
+  auto consume = [&](int tb) {
+    const int st = wi_use % kStages;
+    ok_wait = __all_sync(0xffffffffu, ok_wait && mbar_wait(&full[warp][st], (wi_use / kStages) & 1));
+    ++wi_use;
+    if (!ok_wait) return;
+    const int id = ids[(tb >> lb) - pb0];
+    const bool in_range = id >= 0 && id < a.num_blocks;
+    const uint8_t* src = wring + st * Ring<D>::stage;
+    float kf[U][8], vf[U][8];
+    bool okr[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t kw[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
-      const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+    for (int u = 0; u < U; ++u) {
+      const int r = u * SUBS + sub;
+      okr[u] = in_range && tb + r < t1;
+      const uint4 kw4 = *reinterpret_cast<const uint4*>(src + r * D * 2 + part * 16);
+      const uint4 vw4 = *reinterpret_cast<const uint4*>(src + Ring<D>::box + r * D * 2 + part * 16);
+      const uint32_t kw[4] = {kw4.x, kw4.y, kw4.z, kw4.w};
+      const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float2 fk = unpack2<BF16>(kw[i]);
         float2 fv = unpack2<BF16>(vw[i]);
         kf[u][2 * i] = fk.x;
         kf[u][2 * i + 1] = fk.y;
-        vf[u][2 * i] = fv.x;
-        vf[u][2 * i + 1] = fv.y;
+        vf[u][2 * i] = okr[u] ? fv.x : 0.f;
+        vf[u][2 * i + 1] = okr[u] ? fv.y : 0.f;
       }
     }
-
 #pragma unroll
     for (int j = 0; j < GC; ++j) {
-      float x[kUnroll];
+      float x[U];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         float d = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) d = fmaf(qr[j][i], kf[u][i], d);
@@ -167,12 +219,12 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
 #pragma unroll
       for (int off = TPG / 2; off >= 1; off >>= 1) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) x[u] += __shfl_xor_sync(0xffffffffu, x[u], off);
+        for (int u = 0; u < U; ++u) x[u] += __shfl_xor_sync(0xffffffffu, x[u], off);
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (!ok[u]) x[u] = -INFINITY;
+      for (int u = 0; u < U; ++u) {
+        if (!okr[u]) x[u] = -INFINITY;
         mx = fmaxf(mx, x[u]);
       }
 #pragma unroll
@@ -185,13 +237,51 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[j][i] *= alpha;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         const float pu = exp2f(x[u] - m_new);  // 0 for masked tokens
         l[j] += pu;
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(pu, vf[u][i], acc[j][i]);
       }
     }
+  };
+
+  // Passes of up to kMaxIds blocks (one pass unless the partition is huge).
+  // Warp w takes the 8-token groups w, w + 4, w + 8, ... of the pass.
+  for (;;) {
+    const int pass_t0 = max(t0, pb0 << lb);
+    const int pass_t1 = min(t1, (pb0 + kMaxIds) << lb);
+    const int n_it = pass_t1 > pass_t0 + warp * kRows
+                         ? (pass_t1 - pass_t0 - warp * kRows + kWarps * kRows - 1) / (kWarps * kRows)
+                         : 0;
+    auto tok = [&](int k) { return pass_t0 + (k * kWarps + warp) * kRows; };
+    for (int k = 0; k < n_it && k < kStages; ++k) issue(tok(k));
+    for (int k = 0; k < n_it && ok_wait; ++k) {
+      consume(tok(k));
+      __syncwarp();
+      if (ok_wait && k + kStages < n_it) issue(tok(k + kStages));
+    }
+    if (pass_t1 >= t1) break;
+    // Stage the next pass's block ids (the barrier also makes a timed-out
+    // warp's decision to stop common to the CTA).
+    if (__syncthreads_or(!ok_wait)) {
+      ok_wait = false;
+      break;
+    }
+    pb0 += kMaxIds;
+    const int n = min(blk_end - pb0, kMaxIds);
+    for (int i = threadIdx.x; i < n; i += kThreads) ids[i] = __ldg(bt + pb0 + i);
+    __syncthreads();
+  }
+  if (!ok_wait) {
+    // A bounded wait gave up: report it, and let this warp's loads land
+    // before the CTA can exit.
+    if (lane == 0) {
+      flag(a.status, PKD_DEV_TIMEOUT);
+      for (uint32_t w = wi_use; w < wi_issue; ++w)
+        mbar_wait(&full[warp][w % kStages], (w / kStages) & 1, 100000000ull);
+    }
+    __syncwarp();
   }
 
   // Merge the token rows (subs) of each warp: m is already warp-uniform.
@@ -213,7 +303,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
       dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
     }
   }
-  const bool any_bad = __syncthreads_or(bad);
+  const bool any_bad = __syncthreads_or(bad || !ok_wait);
   if (any_bad && threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_BLOCK);
 
   // Merge the warps and write the result: two output elements per thread.
@@ -249,24 +339,37 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
   }
 }
 
+template <bool BF16, int D, int GC>
+cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
+                     cudaStream_t st) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<BF16, D, GC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<D>::bytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int g = a.num_heads / a.num_kv_heads;
+  dim3 grid(a.num_partitions, a.num_kv_heads * (g / GC), a.num_seqs);
+  decode_simt_kernel<BF16, D, GC><<<grid, kThreads, Ring<D>::bytes, st>>>(km, vm, a);
+  return cudaGetLastError();
+}
+
 template <bool BF16, int D>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t st) {
-  const int g = a.num_heads / a.num_kv_heads;
-  int gc = 1;
-  for (int c : {4, 2, 3, 1}) {
-    if (g % c == 0) {
-      gc = c;
-      break;
-    }
+  CUtensorMap km, vm;
+  const long long rows = (long long)a.num_blocks * a.block_size;
+  if (!make_kv_map(&km, a.key_cache, BF16, D, a.num_kv_heads, rows, D, kRows, false) ||
+      !make_kv_map(&vm, a.value_cache, BF16, D, a.num_kv_heads, rows, D, kRows, false))
+    return cudaErrorInvalidValue;
+  switch (simt_heads_per_cta(a.num_heads / a.num_kv_heads)) {
+    case 4: return launch_g<BF16, D, 4>(a, km, vm, st);
+    case 3: return launch_g<BF16, D, 3>(a, km, vm, st);
+    case 2: return launch_g<BF16, D, 2>(a, km, vm, st);
+    default: return launch_g<BF16, D, 1>(a, km, vm, st);
   }
-  dim3 grid(a.num_partitions, a.num_kv_heads * (g / gc), a.num_seqs);
-  switch (gc) {
-    case 4: decode_simt_kernel<BF16, D, 4><<<grid, kThreads, 0, st>>>(a); break;
-    case 3: decode_simt_kernel<BF16, D, 3><<<grid, kThreads, 0, st>>>(a); break;
-    case 2: decode_simt_kernel<BF16, D, 2><<<grid, kThreads, 0, st>>>(a); break;
-    default: decode_simt_kernel<BF16, D, 1><<<grid, kThreads, 0, st>>>(a); break;
-  }
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -533,50 +533,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
 int pad_group(int g) { return (g + 15) / 16 * 16; }
 
 template <bool BF16, int NPAD>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const cuuint32_t es[3] = {1, 1, 1};
   CUtensorMap km, vm, qm;
-  const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)a.num_kv_heads,
-                              (cuuint64_t)a.num_blocks * a.block_size};
-  const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)a.num_kv_heads * HD * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)(a.block_size < TT ? a.block_size : TT)};
-  if (enc(&km, dt, 3, const_cast<void*>(a.key_cache), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-      enc(&vm, dt, 3, const_cast<void*>(a.value_cache), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  const cuuint64_t qdims[2] = {(cuuint64_t)HD, (cuuint64_t)a.num_seqs * a.num_heads};
-  const cuuint64_t qstrides[1] = {(cuuint64_t)HD * 2};
-  const cuuint32_t qbox[2] = {64, (cuuint32_t)NPAD};
-  if (enc(&qm, dt, 2, const_cast<void*>(a.q), qdims, qstrides, qbox, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const long long rows = (long long)a.num_blocks * a.block_size;
+  const int box_rows = a.block_size < TT ? a.block_size : TT;
+  if (!make_kv_map(&km, a.key_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
+      !make_kv_map(&vm, a.value_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
+      !make_rows_map(&qm, a.q, BF16, HD, (long long)a.num_seqs * a.num_heads, 64, NPAD))
     return cudaErrorInvalidValue;
 
   const int smem = SmemLayout<NPAD>::bytes + 1024;
@@ -611,7 +577,7 @@ cudaError_t launch_b(const DecodeArgs& a, cudaStream_t st) {
 }  // namespace
 
 bool decode_tc_supported(int head_size, int group, int block_size) {
-  return head_size == HD && group >= 4 && group <= 64 && block_size >= 8 && encode_fn() != nullptr;
+  return head_size == HD && group >= 4 && group <= 64 && block_size >= 8 && tma_available();
 }
 
 int decode_tc_tile() { return TT; }

@@ -2,6 +2,7 @@
 // translation units.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -46,6 +47,15 @@ struct CopyArgs {
   int num_blocks;
   uint32_t* status;
 };
+
+// TMA tensor maps (tmap.cu).  KV map: 3-D {head_size, num_kv_heads, rows}
+// over a cache viewed as [rows][num_kv_heads][head_size]; rows map: 2-D
+// {cols, rows}, 128-byte swizzle.
+bool tma_available();
+bool make_kv_map(CUtensorMap* map, const void* cache, bool bf16, int head_size, int num_kv_heads,
+                 long long rows, int box_cols, int box_rows, bool swizzle128);
+bool make_rows_map(CUtensorMap* map, const void* base, bool bf16, int cols, long long rows,
+                   int box_cols, int box_rows);
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 int simt_heads_per_cta(int group);
