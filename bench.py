@@ -46,7 +46,13 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by
 # the sha256 (first 16 hex digits) of the kernel source it was taken on; the
 # value is reported only while that source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # gather_t2048, profiles/gather_cached_kv_t2048.md: 41.97 MB read + 1.83 MB
+    # written during the kernel (its output is still dirty in L2 when it ends)
+    "e1973fa3707e1946": 43794432,
+    # llama13b_mha_b8_ctx256, profiles/decode_simt_llama13b_mha_b8_ctx256.md
+    "a78826731fef997d": 42102272,
+}
 
 
 def env_int(name, default):
