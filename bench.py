@@ -294,6 +294,89 @@ def run_profile(args, local):
     return 0
 
 
+def run_sweep(args, local):
+    """Per-workload device time per call: CUDA-graph replays of 32 calls that
+    rotate over enough input copies to exceed 3x L2 (the same method as the
+    timed region of the default run)."""
+    import torch
+
+    from paged_kv_decode_22_gb300 import ops
+    from paged_kv_decode_22_gb300.workloads import (decode_configs, gather_sweep,
+                                                    make_gather_case)
+    import numpy as np
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peak = FALLBACK_HBM_GBS
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        with open(pk_path) as f:
+            peak = float(json.load(f).get("hbm_gbs") or peak)
+    calls = 32
+
+    def graph_time(fns):
+        """Mean device time per call of the given call list, replayed as a graph."""
+        for fn in fns:
+            fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for i in range(calls):
+                fns[i % len(fns)]()
+        gr.replay()
+        gr.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(5):
+            gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (5 * calls)
+
+    for name in decode_configs():
+        d0 = device_decode_inputs(name, dev)
+        S, H, D = d0["q"].shape
+        Hk, B = d0["kc"].shape[2], d0["kc"].shape[1]
+        ncopy = max(1, min(8, math.ceil(3 * L2_BYTES / d0["bytes"])))
+        sets = [d0] + [dict(d0, q=d0["q"].clone(), kc=d0["kc"].clone(), vc=d0["vc"].clone(),
+                            out=torch.empty_like(d0["out"])) for _ in range(ncopy - 1)]
+        ps, npart, path, ws = ops.decode_plan(S, H, Hk, D, B, d0["max_ctx"])
+        work = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        fns = [lambda d=d: ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"],
+                                                      d["cl"], d["max_ctx"], d["scale"],
+                                                      workspace=work) for d in sets]
+        us = graph_time(fns)
+        print(json.dumps({"workload": name, "kind": "decode", "us_per_call": round(us, 2),
+                          "GBps": round(d0["bytes"] / us / 1e3, 1),
+                          "frac": round(d0["bytes"] / us / 1e3 / peak, 3),
+                          "path": "tc" if path == 1 else "simt", "partitions": npart,
+                          "partition_size": ps, "bytes": d0["bytes"], "copies": ncopy}),
+              flush=True)
+        del d0, sets, work, fns
+        torch.cuda.empty_cache()
+    for name, cfg in gather_sweep().items():
+        g = make_gather_case(name=name, **cfg)
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.float16).to(dev)
+        nb = gather_bytes(g)
+        ncopy = max(1, min(8, math.ceil(3 * L2_BYTES / nb)))
+        sets = []
+        for _ in range(ncopy):
+            ko = torch.empty((g.num_tokens, g.num_heads, g.head_size), dtype=torch.float16,
+                             device=dev)
+            sets.append((ko, torch.empty_like(ko), up(g.key_cache), up(g.value_cache),
+                         torch.from_numpy(g.slot_mapping).to(dev)))
+        fns = [lambda t=t: ops.gather_cached_kv(*t) for t in sets]
+        us = graph_time(fns)
+        print(json.dumps({"workload": name, "kind": "gather", "us_per_call": round(us, 2),
+                          "GBps": round(nb / us / 1e3, 1), "frac": round(nb / us / 1e3 / peak, 3),
+                          "pages_GiBps_one_way": round(nb / 2 / us / 1e3 * 1e9 / 2 ** 30, 1),
+                          "bytes": nb, "copies": ncopy}), flush=True)
+        del sets, fns
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -302,6 +385,8 @@ def main():
     ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
     ap.add_argument("--no-targets", action="store_true", help="skip the large-batch GQA lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every decode workload and gather point (one JSON line each)")
     ap.add_argument("--profile", default=None, metavar="KIND:NAME",
                     help="profiling mode: run only 'decode:<workload>' or 'gather:<workload>' "
                          "warmup + steps times (no timing, no JSON line), e.g. under ncu")
@@ -316,6 +401,8 @@ def main():
         return run_reference(args, world, rank)
     if args.profile:
         return run_profile(args, local)
+    if args.sweep:
+        return run_sweep(args, local)
     import numpy as np
     import torch
 

@@ -64,7 +64,7 @@ struct SmemLayout {
   static constexpr int off_q = off_v + NV * TILE_BYTES;
   static constexpr int off_p = off_q + 2 * QB;
   static constexpr int off_misc = off_p + 2 * QB;
-  static constexpr int misc_bytes = 4608;
+  static constexpr int misc_bytes = 13312;
   static constexpr int bytes = off_misc + misc_bytes;
 };
 
@@ -78,7 +78,13 @@ struct Misc {
   alignas(16) float m_run[64];       // running maxima (log2 domain)
   alignas(16) float alpha[2][64];    // rescale factor of each tile parity
   float lsum[4][64];            // per-warp exponent sums at finalisation
+  // Schedule (sequences <= kSchedMax): lengths and the prefix count of work
+  // units (KV head x non-empty partition) of the sequences before s.
+  int sched_total;
+  int sched_L[1024];
+  int sched_pre[1025];
 };
+constexpr int kSchedMax = 1024;
 
 static_assert(sizeof(Misc) <= SmemLayout<16>::misc_bytes, "misc area too small");
 
@@ -102,6 +108,66 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
   return ui;
 }
 
+__device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
+  return (len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && L > 0)
+             ? (L + a.partition_size - 1) / a.partition_size
+             : 0;
+}
+
+// The units one CTA processes, in order.  With at most kSchedMax sequences the
+// non-empty units are numbered densely (sequence, then KV head, then
+// partition) and each CTA takes an equal contiguous range; otherwise CTAs
+// take units round-robin and skip the empty ones.  Every role of a CTA walks
+// its own copy of the same cursor.
+struct UnitCursor {
+  long long next, end;
+  bool dense;
+};
+
+__device__ __forceinline__ UnitCursor cursor_begin(const Misc& ms, const DecodeArgs& a) {
+  UnitCursor c;
+  c.dense = a.num_seqs <= kSchedMax;
+  if (c.dense) {
+    const long long total = ms.sched_total;
+    c.next = total * blockIdx.x / gridDim.x;
+    c.end = total * (blockIdx.x + 1) / gridDim.x;
+  } else {
+    c.next = blockIdx.x;
+    c.end = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  }
+  return c;
+}
+
+__device__ __forceinline__ bool cursor_next(UnitCursor& c, const Misc& ms, const DecodeArgs& a,
+                                            UnitInfo& ui) {
+  if (c.dense) {
+    if (c.next >= c.end) return false;
+    const int j = (int)c.next++;
+    int lo = 0, hi = a.num_seqs - 1;   // last s with sched_pre[s] <= j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ms.sched_pre[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    ui.s = lo;
+    ui.L = ms.sched_L[lo];
+    const int np = parts_of(a, ui.L);
+    const int r = j - ms.sched_pre[lo];
+    ui.hk = r / np;
+    ui.p = r - ui.hk * np;
+    ui.lok = true;
+    ui.t0 = ui.p * a.partition_size;
+    ui.t1 = min(ui.t0 + a.partition_size, ui.L);
+    ui.ntiles = (ui.t1 - ui.t0 + TT - 1) / TT;
+    return true;
+  }
+  while (c.next < c.end) {
+    ui = unit_info(a, (int)c.next);
+    c.next += gridDim.x;
+    if (ui.ntiles) return true;
+  }
+  return false;
+}
+
 __device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
   ms.abort = 1;
   flag(status, PKD_DEV_TIMEOUT);
@@ -111,12 +177,6 @@ __device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
 // of 128-byte swizzled slabs of 64 columns, `rows` rows per slab.
 __device__ __forceinline__ int sw128_offset(int r, int c, int rows) {
   return (c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1);
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
 }
 
 // Maximum over the 32 lanes of each of 16 per-lane values, by a butterfly
@@ -138,10 +198,21 @@ __device__ __forceinline__ float warp_max16(const float (&v)[16], int lane) {
   return fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Same butterfly for sums: lane l ends with the sum of value (l >> 1) & 15.
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+  float w8[8], w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  for (int i = 0; i < 8; ++i)
+    w8[i] = (b4 ? v[8 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[8 + i], 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w4[i] = (b3 ? w8[4 + i] : w8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? w8[i] : w8[4 + i], 8);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    w2[i] = (b2 ? w4[2 + i] : w4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? w4[i] : w4[2 + i], 4);
+  float w1 = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
+  return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
 }
 
 template <bool BF16, int NPAD>
@@ -162,7 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = a.num_heads / a.num_kv_heads;
-  const int n_units = a.num_seqs * a.num_kv_heads * a.num_partitions;
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -197,6 +267,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ms.tmem_base, tmem_cols(NPAD));
     tmem_relinquish();
   }
+  // Schedule: per-sequence unit counts, then an exclusive prefix sum by warp 0.
+  if (a.num_seqs <= kSchedMax) {
+    for (int i = threadIdx.x; i < a.num_seqs; i += kThreads) {
+      const int L = a.context_lens[i];
+      ms.sched_L[i] = L;
+      ms.sched_pre[i + 1] = parts_of(a, L) * a.num_kv_heads;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base < a.num_seqs; base += 32) {
+        int v = base + lane < a.num_seqs ? ms.sched_pre[base + lane + 1] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += n;
+        }
+        if (base + lane < a.num_seqs) ms.sched_pre[base + lane + 1] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) {
+        ms.sched_pre[0] = 0;
+        ms.sched_total = carry;
+      }
+    }
+  }
+  // Sequences with nothing to attend to: zero rows (unsplit; the merge writes
+  // them when split) and the length status bit.
+  for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
+    const int L = a.context_lens[sq];
+    if (parts_of(a, L) == 0) {
+      if (!len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && threadIdx.x == 0)
+        flag(a.status, PKD_DEV_BAD_LEN);
+      if (a.num_partitions == 1) {
+        uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)sq * a.num_heads * HD / 2;
+        for (int i = threadIdx.x; i < a.num_heads * HD / 2; i += kThreads) o[i] = 0u;
+      }
+    }
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -219,13 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool issuer = lane < 2 * nbox;      // lane issues box (lane % nbox) of half (lane / nbox)
     const int my_box = lane % nbox, my_half = lane / nbox;
 
-    auto next_unit = [&](int from, UnitInfo& out) {
-      for (int x = from; x < n_units; x += gridDim.x) {
-        out = unit_info(a, x);
-        if (out.ntiles) return x;
-      }
-      return n_units;
-    };
     // Raw block id of box `lane` of tile tj (lanes < nbox), kNoBlock if the
     // box lies past the partition end.  The loaded value is first used one
     // tile later, so its latency hides behind the current tile's issue.
@@ -238,19 +340,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return raw;
     };
+    UnitCursor cur = cursor_begin(ms, a);
     UnitInfo ui;
-    int u = next_unit(blockIdx.x, ui), jl = 0;
-    int raw = u < n_units ? load_raw(ui, 0) : kNoBlock;
+    bool have = cursor_next(cur, ms, a, ui);
+    int jl = 0;
+    int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
     bool ok = true;
-    while (u < n_units) {
+    while (have) {
       UnitInfo nui = ui;
-      int nu = u, njl = jl + 1;
+      bool nhave = true;
+      int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nu = next_unit(u + gridDim.x, nui);
+        nhave = cursor_next(cur, ms, a, nui);
         njl = 0;
       }
-      const int nraw = nu < n_units ? load_raw(nui, njl) : kNoBlock;
+      const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
       if (!is_v && jl == 0 && lane == 0) {
         const int qb = un & 1;
         ok = mbar_wait(&ms.q_empty[qb], ((un >> 1) & 1) ^ 1);
@@ -283,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_hint(ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128, map,
                          &full[st], my_half * 64, ui.hk, r, policy);
       ++jk;
-      if (nu != u) ++un;
-      u = nu;
+      if (njl == 0) ++un;
+      have = nhave;
       ui = nui;
       jl = njl;
       raw = nraw;
@@ -323,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&ms.o_full[b]);
         mma_commit(&ms.v_empty[vs]);
       };
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const UnitInfo ui = unit_info(a, u);
-        if (ui.ntiles == 0) continue;
+      UnitCursor cur = cursor_begin(ms, a);
+      UnitInfo ui;
+      while (ok && cursor_next(cur, ms, a, ui)) {
         const int qb = un & 1;
         ok = mbar_wait(&ms.q_full[qb], (un >> 1) & 1);
         for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++j) {
@@ -378,28 +483,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < NPAD / 16; ++c) {
-        float v[16];
+        float v[16], al[16];
         tmem_ld16(lane_addr + 2 * NPAD + b * NPAD + c * 16, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int h = c * 16 + i;
-          o_acc[h] = fmaf(o_acc[h], ms.alpha[b][h], v[i]);
-        }
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(&al[i]) = *reinterpret_cast<const float4*>(&ms.alpha[b][c * 16 + i]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o_acc[c * 16 + i] = fmaf(o_acc[c * 16 + i], al[i], v[i]);
       }
       tc_fence_before();
     };
 
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const UnitInfo ui = unit_info(a, u);
+    UnitCursor cur = cursor_begin(ms, a);
+    UnitInfo ui;
+    while (ok && cursor_next(cur, ms, a, ui)) {
       const int h0 = ui.hk * g;
-      if (ui.ntiles == 0) {
-        if (single) {
-          uint16_t* o = reinterpret_cast<uint16_t*>(a.out);
-          for (int h = 0; h < g; ++h) o[((size_t)ui.s * H + h0 + h) * HD + row] = 0;
-        }
-        if (!ui.lok && ui.p == 0 && ui.hk == 0 && row == 0) flag(a.status, PKD_DEV_BAD_LEN);
-        continue;
-      }
       bool unit_bad = false;
       // Every wait below is bounded; a thread that gives up keeps taking part
       // in the group barriers, which AND the flag so the group stops together.
@@ -481,11 +579,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // ---------------------------------------------------------- finalise unit
 #pragma unroll
-      for (int h = 0; h < NPAD; ++h) {
-        if (h < g) {
-          const float t = warp_sum(l_part[h]);
-          if (lane == 0) ms.lsum[wq][h] = t;
-        }
+      for (int c = 0; c < NPAD / 16; ++c) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = l_part[c * 16 + i];
+        const float t = warp_sum16(v, lane);
+        if ((lane & 1) == 0) ms.lsum[wq][c * 16 + (lane >> 1)] = t;
       }
       ok = named_barrier_and(kSoftmaxBar, kSoftmaxThreads, ok);
       if (!ok) break;
