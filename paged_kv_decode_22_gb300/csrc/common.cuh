@@ -60,6 +60,26 @@ __device__ __forceinline__ bool len_ok(int L, int max_context_len, int max_block
          (long long)L <= (long long)max_blocks_per_seq * block_size;
 }
 
+// Row of the split-context workspace holding the partial result of query
+// head h of sequence s over context partition p.  Rows are ordered
+// [sequence][KV head][partition][head within the group], so the partials of
+// one (sequence, KV head, partition) unit form one contiguous block.
+__device__ __forceinline__ size_t partial_row(int s, int h, int p, int num_heads, int num_kv_heads,
+                                              int num_partitions) {
+  const int g = num_heads / num_kv_heads;
+  const int hk = h / g;
+  return (((size_t)s * num_kv_heads + hk) * num_partitions + p) * g + (h - hk * g);
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22, results below 2^-126 flushed to zero, 2^-inf = 0).  Softmax
+// weights need no more.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 }  // namespace pkd

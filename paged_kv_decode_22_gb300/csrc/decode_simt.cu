@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads)
       reinterpret_cast<uint32_t*>(a.out)[(((size_t)s * H + h) * D + d) / 2] =
           pack2<BF16>(n0 * inv, n1 * inv);
     } else {
-      const size_t sp = ((size_t)s * H + h) * a.num_partitions + p;
+      const size_t sp = partial_row(s, h, p, H, a.num_kv_heads, a.num_partitions);
       *reinterpret_cast<float2*>(&a.ws_o[sp * D + d]) = make_float2(n0, n1);
       if (d == 0) {
         a.ws_m[sp] = M;

@@ -78,6 +78,8 @@ struct Misc {
   alignas(16) float m_run[64];       // running maxima (log2 domain)
   alignas(16) float alpha[2][64];    // rescale factor of each tile parity
   float lsum[4][64];            // per-warp exponent sums at finalisation
+  alignas(16) float inv_l[64];       // 1 / sum (0 for a bad unit)
+  float sum_l[64];                   // sum written to the workspace
   // Schedule (sequences <= kSchedMax): lengths and the prefix count of work
   // units (KV head x non-empty partition) of the sequences before s.
   int sched_total;
@@ -431,8 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       UnitCursor cur = cursor_begin(ms, a);
       UnitInfo ui;
       while (ok && cursor_next(cur, ms, a, ui)) {
+        // The softmax warps finish the previous unit only after its last P V:
+        // issue that one before this unit's first S.
+        if (prev >= 0) {
+          issue_pv((uint32_t)prev);
+          prev = -1;
+        }
         const int qb = un & 1;
-        ok = mbar_wait(&ms.q_full[qb], (un >> 1) & 1);
+        ok = ok && mbar_wait(&ms.q_full[qb], (un >> 1) & 1);
         for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++j) {
           const int ks = j % NK, b = j & 1;
           ok = mbar_wait(&ms.k_full[ks], (j / NK) & 1);
@@ -533,9 +541,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  fmaxf(ms.red[b][2][et], ms.red[b][3][et]));
           const float m_old = ms.m_run[et];
           const float m_new = fmaxf(m_old, mt);
-          ms.alpha[b][et] = m_new == -INFINITY ? 1.f : exp2f(m_old - m_new);
+          ms.alpha[b][et] = m_new == -INFINITY ? 1.f : fast_exp2(m_old - m_new);
           ms.m_run[et] = m_new;
         }
+        // A unit's output may still be read from the P buffers by its bulk
+        // store: let it finish before they are overwritten.
+        if (threadIdx.x == 64) bulk_wait_read_all();
         named_barrier(kSoftmaxBar, kSoftmaxThreads);
         // Probabilities: written 16-bit into the P^T operand, summed per thread.
         uint8_t* pb = pbuf + b * LY::QB;
@@ -550,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             const int h = c * 16 + i;
-            const float p0 = (valid && h < g) ? exp2f(xs[h] - mr[i]) : 0.f;
-            const float p1 = (valid && h + 1 < g) ? exp2f(xs[h + 1] - mr[i + 1]) : 0.f;
+            const float p0 = (valid && h < g) ? fast_exp2(xs[h] - mr[i]) : 0.f;
+            const float p1 = (valid && h + 1 < g) ? fast_exp2(xs[h + 1] - mr[i + 1]) : 0.f;
             l_part[h] = fmaf(l_part[h], al[i], p0);
             l_part[h + 1] = fmaf(l_part[h + 1], al[i + 1], p1);
             const uint32_t pk = pack2<BF16>(p0, p1);
@@ -588,32 +599,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = named_barrier_and(kSoftmaxBar, kSoftmaxThreads, ok);
       if (!ok) break;
-      const size_t sp0 = (size_t)ui.s * H + h0;
-      if (single) {
-        uint16_t* o = reinterpret_cast<uint16_t*>(a.out);
-#pragma unroll
-        for (int h = 0; h < NPAD; ++h) {
-          if (h < g) {
-            const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
-            const float v = unit_bad ? 0.f : o_acc[h] / den;
-            o[(sp0 + h) * HD + row] = (uint16_t)pack2<BF16>(v, 0.f);
-          }
-        }
-      } else {
-        const int P = a.num_partitions;
-#pragma unroll
-        for (int h = 0; h < NPAD; ++h) {
-          if (h < g) a.ws_o[((sp0 + h) * P + ui.p) * HD + row] = o_acc[h];
-        }
-        const int et = threadIdx.x - 64;
-        if (et < g) {
-          const float den = ms.lsum[0][et] + ms.lsum[1][et] + ms.lsum[2][et] + ms.lsum[3][et];
-          a.ws_m[(sp0 + et) * P + ui.p] = ms.m_run[et];
-          a.ws_l[(sp0 + et) * P + ui.p] = unit_bad ? -1.f : den;
-        }
+      // Stage the unit's result in the P buffers (idle now: the unit's last
+      // P V has completed and the next P is written after this) and write it
+      // with one bulk copy: g rows of the output, or of the workspace.
+      const int et = threadIdx.x - 64;
+      if (et < g) {
+        const float den = ms.lsum[0][et] + ms.lsum[1][et] + ms.lsum[2][et] + ms.lsum[3][et];
+        ms.inv_l[et] = unit_bad || den == 0.f ? 0.f : 1.f / den;
+        ms.sum_l[et] = unit_bad ? -1.f : den;
       }
       named_barrier(kSoftmaxBar, kSoftmaxThreads);
-      const int et = threadIdx.x - 64;
+      const size_t unit_row = (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
+      if (single) {
+        uint16_t* st = reinterpret_cast<uint16_t*>(pbuf);
+#pragma unroll
+        for (int h = 0; h < NPAD; ++h)
+          if (h < g) st[h * HD + row] = (uint16_t)pack2<BF16>(o_acc[h] * ms.inv_l[h], 0.f);
+      } else {
+        float* st = reinterpret_cast<float*>(pbuf);
+#pragma unroll
+        for (int h = 0; h < NPAD; ++h)
+          if (h < g) st[h * HD + row] = o_acc[h];
+        if (et < g) {
+          a.ws_m[unit_row + et] = ms.m_run[et];
+          a.ws_l[unit_row + et] = ms.sum_l[et];
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier(kSoftmaxBar, kSoftmaxThreads);
+      if (threadIdx.x == 64) {
+        if (single)
+          bulk_store(reinterpret_cast<uint16_t*>(a.out) + ((size_t)ui.s * H + h0) * HD, pbuf,
+                     (uint32_t)(g * HD * 2));
+        else
+          bulk_store(a.ws_o + unit_row * HD, pbuf, (uint32_t)(g * HD * 4));
+        bulk_commit();          // waited for before the next P is written
+      }
       if (et < 64) ms.m_run[et] = -INFINITY;
 #pragma unroll
       for (int h = 0; h < NPAD; ++h) o_acc[h] = l_part[h] = 0.f;
@@ -622,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  if (threadIdx.x == 64) bulk_wait_all();   // output stores complete before exit
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

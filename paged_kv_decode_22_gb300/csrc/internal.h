@@ -29,9 +29,9 @@ struct DecodeArgs {
   int is_bf16;
   int partition_size;   // tokens per partition (multiple of 64)
   int num_partitions;   // 1 = write `out` directly
-  float* ws_o;          // [S][H][P][D] unnormalised partial outputs
-  float* ws_m;          // [S][H][P] partial maxima (log2 domain)
-  float* ws_l;          // [S][H][P] partial sums; < 0 marks a bad block
+  float* ws_o;          // [S][Hk][P][H/Hk][D] unnormalised partial outputs
+  float* ws_m;          // [S][Hk][P][H/Hk] partial maxima (log2 domain)
+  float* ws_l;          // [S][Hk][P][H/Hk] partial sums; < 0 marks a bad block
   uint32_t* status;
 };
 

@@ -34,14 +34,17 @@ __global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(const DecodeArg
   const int L = a.context_lens[s];
   const bool lok = len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
   const int n_p = lok ? (L + a.partition_size - 1) / a.partition_size : 0;
-  const float* ms = a.ws_m + sh * P;
-  const float* ls = a.ws_l + sh * P;
+  // Partials of (s, h) sit g rows apart, one per partition.
+  const int g = H / a.num_kv_heads;
+  const size_t row0 = partial_row(s, (int)(sh - (long long)s * H), 0, H, a.num_kv_heads, P);
+  const float* ms = a.ws_m + row0;
+  const float* ls = a.ws_l + row0;
 
   float M = -INFINITY;
   bool bad = false;
   for (int p = lane; p < n_p; p += 32) {
-    M = fmaxf(M, ms[p]);
-    bad |= ls[p] < 0.f;
+    M = fmaxf(M, ms[(size_t)p * g]);
+    bad |= ls[(size_t)p * g] < 0.f;
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -52,18 +55,18 @@ __global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(const DecodeArg
   for (int i = 0; i < E; ++i) acc[i] = 0.f;
   float den = 0.f;
   if (!bad && M != -INFINITY) {
-    const float* os = a.ws_o + sh * P * D + lane * E;
+    const float* os = a.ws_o + row0 * D + lane * E;
     for (int p = 0; p < n_p; ++p) {
-      const float w = exp2f(ms[p] - M);
-      den = fmaf(w, ls[p], den);
+      const float w = exp2f(ms[(size_t)p * g] - M);
+      den = fmaf(w, ls[(size_t)p * g], den);
       if constexpr (E == 4) {
-        const float4 o = *reinterpret_cast<const float4*>(os + (size_t)p * D);
+        const float4 o = *reinterpret_cast<const float4*>(os + (size_t)p * g * D);
         acc[0] = fmaf(w, o.x, acc[0]);
         acc[1] = fmaf(w, o.y, acc[1]);
         acc[2] = fmaf(w, o.z, acc[2]);
         acc[3] = fmaf(w, o.w, acc[3]);
       } else {
-        const float2 o = *reinterpret_cast<const float2*>(os + (size_t)p * D);
+        const float2 o = *reinterpret_cast<const float2*>(os + (size_t)p * g * D);
         acc[0] = fmaf(w, o.x, acc[0]);
         acc[1] = fmaf(w, o.y, acc[1]);
       }
