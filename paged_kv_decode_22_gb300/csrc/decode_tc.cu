@@ -42,14 +42,16 @@ using namespace sm100;
 constexpr int TT = 128;                 // tokens per tile (= MMA M for S)
 constexpr int HD = 128;                 // head_size of this path (= MMA M for O)
 constexpr int TILE_BYTES = TT * HD * 2; // one K or V tile, 32 KB
-constexpr int kThreads = 224;          // 7 warps, roles below
-constexpr int kVWarp = 6;              // V producer (warp 0 produces K and q)
-constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxThreads = 128;   // one softmax warpgroup
 constexpr int kNoBlock = -2147483647 - 1;  // "no block here" marker of the producers
-constexpr uint32_t kSoftmaxBar = 1;     // named barrier id of warps 2-5
+constexpr uint32_t kSoftmaxBar = 1;     // named barrier id of softmax group 0 (group 1: 2)
 
 __host__ __device__ constexpr int k_stages(int npad) { return npad <= 48 ? 3 : 2; }
 __host__ __device__ constexpr int v_stages(int npad) { return npad <= 16 ? 3 : 2; }
+// Query heads of a group are split between 1 or 2 softmax warpgroups; each
+// handles HPG heads in chunks of CH columns.
+__host__ __device__ constexpr int sm_groups(int npad) { return npad >= 32 ? 2 : 1; }
+__host__ __device__ constexpr int threads_of(int npad) { return 64 + 128 * sm_groups(npad) + 32; }
 __host__ __device__ constexpr int tmem_cols(int npad) {
   return 4 * npad <= 32 ? 32 : 4 * npad <= 64 ? 64 : 4 * npad <= 128 ? 128 : 256;
 }
@@ -200,6 +202,35 @@ __device__ __forceinline__ float warp_max16(const float (&v)[16], int lane) {
   return fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
 }
 
+// 8-value versions: lane l ends with the result for value (l >> 2) & 7.
+__device__ __forceinline__ float warp_max8(const float (&v)[8], int lane) {
+  float w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w4[i] = fmaxf(b4 ? v[4 + i] : v[i], __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16));
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    w2[i] = fmaxf(b3 ? w4[2 + i] : w4[i], __shfl_xor_sync(0xffffffffu, b3 ? w4[i] : w4[2 + i], 8));
+  float w1 = fmaxf(b2 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4));
+  w1 = fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 2));
+  return fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
+}
+
+__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
+  float w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w4[i] = (b4 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    w2[i] = (b3 ? w4[2 + i] : w4[i]) + __shfl_xor_sync(0xffffffffu, b3 ? w4[i] : w4[2 + i], 8);
+  float w1 = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+  w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
+  return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
+}
+
 // Same butterfly for sums: lane l ends with the sum of value (l >> 1) & 15.
 __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
   float w8[8], w4[4], w2[2];
@@ -217,13 +248,36 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
   return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
 }
 
+template <int CH>
+__device__ __forceinline__ float chunk_max(const float (&v)[CH], int lane) {
+  if constexpr (CH == 16) return warp_max16(v, lane); else return warp_max8(v, lane);
+}
+template <int CH>
+__device__ __forceinline__ float chunk_sum(const float (&v)[CH], int lane) {
+  if constexpr (CH == 16) return warp_sum16(v, lane); else return warp_sum8(v, lane);
+}
+// Lane that holds a chunk reduction's result for value i, and the value a lane holds.
+template <int CH>
+__device__ __forceinline__ bool chunk_writer(int lane) { return (lane & (32 / CH - 1)) == 0; }
+template <int CH>
+__device__ __forceinline__ int chunk_index(int lane) { return (lane / (32 / CH)) & (CH - 1); }
+
+template <int CH>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[CH]) {
+  if constexpr (CH == 16) tmem_ld16(taddr, v); else tmem_ld8(taddr, v);
+}
+
+
 template <bool BF16, int NPAD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(NPAD), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
   using LY = SmemLayout<NPAD>;
   constexpr int NK = LY::NK, NV = LY::NV;
+  constexpr int GROUPS = sm_groups(NPAD);
+  constexpr int kThreads = threads_of(NPAD);
+  constexpr int kVWarp = 2 + 4 * GROUPS;     // V producer (warp 0 produces K and q)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -240,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) {
       mbar_init(&ms.k_full[i], 1);
-      mbar_init(&ms.k_empty[i], 1 + kSoftmaxThreads);
+      mbar_init(&ms.k_empty[i], 1 + kSoftmaxThreads * GROUPS);
       ms.k_bad[i] = 0;
     }
     for (int i = 0; i < NV; ++i) {
@@ -251,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ms.q_full[i], 1);
       mbar_init(&ms.q_empty[i], 1);
       mbar_init(&ms.s_full[i], 1);
-      mbar_init(&ms.p_full[i], kSoftmaxThreads);
+      mbar_init(&ms.p_full[i], kSoftmaxThreads * GROUPS);
       mbar_init(&ms.o_full[i], 1);
     }
     mbar_init(&ms.drain, 1);
@@ -472,15 +526,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ============================================================ softmax / epilogue
+    // Softmax warpgroup grp handles query heads [hbase, hbase + HPG) of the
+    // group, in chunks of CH: its own maxima, probabilities, P rows, O columns
+    // and output rows, with its own named barrier.  Heads are independent, so
+    // the warpgroups never wait for each other.
+    constexpr int HPG = NPAD / GROUPS;
+    constexpr int CH = HPG % 16 == 0 ? 16 : 8;
+    constexpr int NCH = HPG / CH;
+    const int grp = (warp - 2) >> 2;
+    const int hbase = grp * HPG;
+    const uint32_t bar = kSoftmaxBar + grp;
+    const int et = threadIdx.x - 64 - kSoftmaxThreads * grp;   // thread within the warpgroup
+    const bool leader = et == 0;
     const int wq = warp & 3;                   // TMEM lane quadrant of this warp
     const int row = wq * 32 + lane;            // token row of S, d row of O
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float qscale = a.scale * kLog2e;
     const bool single = a.num_partitions == 1;
     const int H = a.num_heads;
-    float o_acc[NPAD], l_part[NPAD];
+    const int my_heads = max(0, min(HPG, g - hbase));    // valid heads of this warpgroup
+    float o_acc[HPG], l_part[HPG];
 #pragma unroll
-    for (int h = 0; h < NPAD; ++h) o_acc[h] = l_part[h] = 0.f;
+    for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
     uint32_t j = 0;
     bool ok = true;
 
@@ -490,14 +557,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) return;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < NPAD / 16; ++c) {
-        float v[16], al[16];
-        tmem_ld16(lane_addr + 2 * NPAD + b * NPAD + c * 16, v);
+      for (int c = 0; c < NCH; ++c) {
+        float v[CH], al[CH];
+        tmem_ld<CH>(lane_addr + 2 * NPAD + b * NPAD + hbase + c * CH, v);
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(&al[i]) = *reinterpret_cast<const float4*>(&ms.alpha[b][c * 16 + i]);
+        for (int i = 0; i < CH; i += 4)
+          *reinterpret_cast<float4*>(&al[i]) =
+              *reinterpret_cast<const float4*>(&ms.alpha[b][hbase + c * CH + i]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o_acc[c * 16 + i] = fmaf(o_acc[c * 16 + i], al[i], v[i]);
+        for (int i = 0; i < CH; ++i) o_acc[c * CH + i] = fmaf(o_acc[c * CH + i], al[i], v[i]);
       }
       tc_fence_before();
     };
@@ -519,61 +587,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         unit_bad |= ms.k_bad[ks] != 0;
         mbar_arrive(&ms.k_empty[ks]);
         // Tile maxima per head (logits kept in registers for the exponentials).
-        const uint32_t s_addr = lane_addr + b * NPAD;
-        float xs[NPAD];
+        const uint32_t s_addr = lane_addr + b * NPAD + hbase;
+        float xs[HPG];
 #pragma unroll
-        for (int c = 0; c < NPAD / 16; ++c) {
-          float x[16];
-          tmem_ld16(s_addr + c * 16, x);
+        for (int c = 0; c < NCH; ++c) {
+          float x[CH];
+          tmem_ld<CH>(s_addr + c * CH, x);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < CH; ++i) {
             x[i] = valid ? x[i] * qscale : -INFINITY;
-            xs[c * 16 + i] = x[i];
+            xs[c * CH + i] = x[i];
           }
-          const float m = warp_max16(x, lane);
-          if ((lane & 1) == 0) ms.red[b][wq][c * 16 + (lane >> 1)] = m;
+          const float m = chunk_max<CH>(x, lane);
+          if (chunk_writer<CH>(lane)) ms.red[b][wq][hbase + c * CH + chunk_index<CH>(lane)] = m;
         }
-        ok = named_barrier_and(kSoftmaxBar, kSoftmaxThreads, ok);
+        ok = named_barrier_and(bar, kSoftmaxThreads, ok);
         if (!ok) break;
-        const int et = threadIdx.x - 64;
-        if (et < g) {
-          const float mt = fmaxf(fmaxf(ms.red[b][0][et], ms.red[b][1][et]),
-                                 fmaxf(ms.red[b][2][et], ms.red[b][3][et]));
-          const float m_old = ms.m_run[et];
+        if (et < my_heads) {
+          const int h = hbase + et;
+          const float mt = fmaxf(fmaxf(ms.red[b][0][h], ms.red[b][1][h]),
+                                 fmaxf(ms.red[b][2][h], ms.red[b][3][h]));
+          const float m_old = ms.m_run[h];
           const float m_new = fmaxf(m_old, mt);
-          ms.alpha[b][et] = m_new == -INFINITY ? 1.f : fast_exp2(m_old - m_new);
-          ms.m_run[et] = m_new;
+          ms.alpha[b][h] = m_new == -INFINITY ? 1.f : fast_exp2(m_old - m_new);
+          ms.m_run[h] = m_new;
         }
-        // A unit's output may still be read from the P buffers by its bulk
-        // store: let it finish before they are overwritten.
-        if (threadIdx.x == 64) bulk_wait_read_all();
-        named_barrier(kSoftmaxBar, kSoftmaxThreads);
+        // A unit's output may still be read from this warpgroup's P rows by
+        // its bulk stores: let them finish before the rows are overwritten.
+        if (leader) bulk_wait_read_all();
+        named_barrier(bar, kSoftmaxThreads);
         // Probabilities: written 16-bit into the P^T operand, summed per thread.
         uint8_t* pb = pbuf + b * LY::QB;
 #pragma unroll
-        for (int c = 0; c < NPAD / 16; ++c) {
-          float mr[16], al[16];
+        for (int c = 0; c < NCH; ++c) {
+          float mr[CH], al[CH];
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            *reinterpret_cast<float4*>(&mr[i]) = *reinterpret_cast<const float4*>(&ms.m_run[c * 16 + i]);
-            *reinterpret_cast<float4*>(&al[i]) = *reinterpret_cast<const float4*>(&ms.alpha[b][c * 16 + i]);
+          for (int i = 0; i < CH; i += 4) {
+            *reinterpret_cast<float4*>(&mr[i]) =
+                *reinterpret_cast<const float4*>(&ms.m_run[hbase + c * CH + i]);
+            *reinterpret_cast<float4*>(&al[i]) =
+                *reinterpret_cast<const float4*>(&ms.alpha[b][hbase + c * CH + i]);
           }
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const int h = c * 16 + i;
-            const float p0 = (valid && h < g) ? fast_exp2(xs[h] - mr[i]) : 0.f;
-            const float p1 = (valid && h + 1 < g) ? fast_exp2(xs[h + 1] - mr[i + 1]) : 0.f;
-            l_part[h] = fmaf(l_part[h], al[i], p0);
-            l_part[h + 1] = fmaf(l_part[h + 1], al[i + 1], p1);
+          for (int i = 0; i < CH; i += 2) {
+            const int hl = c * CH + i;          // head within the warpgroup
+            const int h = hbase + hl;
+            const float p0 = (valid && hl < my_heads) ? fast_exp2(xs[hl] - mr[i]) : 0.f;
+            const float p1 = (valid && hl + 1 < my_heads) ? fast_exp2(xs[hl + 1] - mr[i + 1]) : 0.f;
+            l_part[hl] = fmaf(l_part[hl], al[i], p0);
+            l_part[hl + 1] = fmaf(l_part[hl + 1], al[i + 1], p1);
             const uint32_t pk = pack2<BF16>(p0, p1);
-            if (h < g) *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row, NPAD)) = (uint16_t)pk;
-            if (h + 1 < g)
+            if (hl < my_heads)
+              *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row, NPAD)) = (uint16_t)pk;
+            if (hl + 1 < my_heads)
               *reinterpret_cast<uint16_t*>(pb + sw128_offset(h + 1, row, NPAD)) = (uint16_t)(pk >> 16);
           }
         }
         // Cache slots past the sequence end inside a loaded block may hold
         // anything (NaN included): zero those V rows before P V reads them.
-        if (ts + TT > ui.L) {
+        // (Warpgroup 0 does it; the others' arrivals on p_full come after
+        // theirs, and P V waits for all of them.)
+        if (ts + TT > ui.L && grp == 0) {
           ok = ok && mbar_wait(&ms.v_full[vs], (j / NV) & 1);
           if (ok && ts + row >= ui.L) {
             uint4* v0 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + row * 128);
@@ -590,60 +664,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // ---------------------------------------------------------- finalise unit
 #pragma unroll
-      for (int c = 0; c < NPAD / 16; ++c) {
-        float v[16];
+      for (int c = 0; c < NCH; ++c) {
+        float v[CH];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = l_part[c * 16 + i];
-        const float t = warp_sum16(v, lane);
-        if ((lane & 1) == 0) ms.lsum[wq][c * 16 + (lane >> 1)] = t;
+        for (int i = 0; i < CH; ++i) v[i] = l_part[c * CH + i];
+        const float t = chunk_sum<CH>(v, lane);
+        if (chunk_writer<CH>(lane)) ms.lsum[wq][hbase + c * CH + chunk_index<CH>(lane)] = t;
       }
-      ok = named_barrier_and(kSoftmaxBar, kSoftmaxThreads, ok);
+      ok = named_barrier_and(bar, kSoftmaxThreads, ok);
       if (!ok) break;
-      // Stage the unit's result in the P buffers (idle now: the unit's last
-      // P V has completed and the next P is written after this) and write it
-      // with one bulk copy: g rows of the output, or of the workspace.
-      const int et = threadIdx.x - 64;
-      if (et < g) {
-        const float den = ms.lsum[0][et] + ms.lsum[1][et] + ms.lsum[2][et] + ms.lsum[3][et];
-        ms.inv_l[et] = unit_bad || den == 0.f ? 0.f : 1.f / den;
-        ms.sum_l[et] = unit_bad ? -1.f : den;
+      if (et < my_heads) {
+        const int h = hbase + et;
+        const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
+        ms.inv_l[h] = unit_bad || den == 0.f ? 0.f : 1.f / den;
+        ms.sum_l[h] = unit_bad ? -1.f : den;
       }
-      named_barrier(kSoftmaxBar, kSoftmaxThreads);
+      named_barrier(bar, kSoftmaxThreads);
+      // Stage this warpgroup's output rows in its own P rows (idle now: the
+      // unit's last P V has completed) and write them with bulk copies.  The
+      // warpgroup's P rows are four pieces of HPG x 128 bytes (2 buffers x 2
+      // slabs); a piece holds HPG/4 whole fp32 rows of the workspace, or with
+      // 16-bit output the first two pieces hold HPG/2 output rows each.
       const size_t unit_row = (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
+      auto piece = [&](int q) { return pbuf + (q >> 1) * LY::QB + (q & 1) * NPAD * 128 + hbase * 128; };
       if (single) {
-        uint16_t* st = reinterpret_cast<uint16_t*>(pbuf);
+        constexpr int per = HPG / 2;            // output rows per piece
 #pragma unroll
-        for (int h = 0; h < NPAD; ++h)
-          if (h < g) st[h * HD + row] = (uint16_t)pack2<BF16>(o_acc[h] * ms.inv_l[h], 0.f);
+        for (int hl = 0; hl < HPG; ++hl) {
+          if (hl < my_heads) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(piece(hl / per)) + (hl % per) * HD + row;
+            *dst = (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[hbase + hl], 0.f);
+          }
+        }
       } else {
-        float* st = reinterpret_cast<float*>(pbuf);
+        constexpr int per = HPG / 4;            // workspace rows per piece
 #pragma unroll
-        for (int h = 0; h < NPAD; ++h)
-          if (h < g) st[h * HD + row] = o_acc[h];
-        if (et < g) {
-          a.ws_m[unit_row + et] = ms.m_run[et];
-          a.ws_l[unit_row + et] = ms.sum_l[et];
+        for (int hl = 0; hl < HPG; ++hl) {
+          if (hl < my_heads) reinterpret_cast<float*>(piece(hl / per))[(hl % per) * HD + row] = o_acc[hl];
+        }
+        if (et < my_heads) {
+          a.ws_m[unit_row + hbase + et] = ms.m_run[hbase + et];
+          a.ws_l[unit_row + hbase + et] = ms.sum_l[hbase + et];
         }
       }
       fence_proxy_async_smem();
-      named_barrier(kSoftmaxBar, kSoftmaxThreads);
-      if (threadIdx.x == 64) {
-        if (single)
-          bulk_store(reinterpret_cast<uint16_t*>(a.out) + ((size_t)ui.s * H + h0) * HD, pbuf,
-                     (uint32_t)(g * HD * 2));
-        else
-          bulk_store(a.ws_o + unit_row * HD, pbuf, (uint32_t)(g * HD * 4));
-        bulk_commit();          // waited for before the next P is written
+      named_barrier(bar, kSoftmaxThreads);
+      if (leader) {
+        const int per = single ? HPG / 2 : HPG / 4;
+        const int esz = single ? 2 : 4;
+        for (int q = 0; q * per < my_heads; ++q) {
+          const int n = min(per, my_heads - q * per);
+          const size_t r0 = single ? (size_t)ui.s * H + h0 + hbase + q * per : unit_row + hbase + q * per;
+          char* dst = single ? reinterpret_cast<char*>(a.out) : reinterpret_cast<char*>(a.ws_o);
+          bulk_store(dst + r0 * HD * esz, piece(q), (uint32_t)(n * HD * esz));
+        }
+        bulk_commit();          // waited for before this warpgroup's next P rows
       }
-      if (et < 64) ms.m_run[et] = -INFINITY;
+      if (et < my_heads) ms.m_run[hbase + et] = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < NPAD; ++h) o_acc[h] = l_part[h] = 0.f;
+      for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
     }
-    if (!ok && threadIdx.x == 64) set_abort(ms, a.status);
+    if (!ok && leader) set_abort(ms, a.status);
   }
 
   // ---------------------------------------------------------------- teardown
-  if (threadIdx.x == 64) bulk_wait_all();   // output stores complete before exit
+  if (warp >= 2 && warp < kVWarp && ((threadIdx.x - 64) & (kSoftmaxThreads - 1)) == 0)
+    bulk_wait_all();   // output stores complete before exit
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -680,7 +766,7 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   const int grid = (int)(units < sms ? units : sms);
-  decode_tc_kernel<BF16, NPAD><<<grid, kThreads, smem, st>>>(km, vm, qm, a);
+  decode_tc_kernel<BF16, NPAD><<<grid, threads_of(NPAD), smem, st>>>(km, vm, qm, a);
   return cudaGetLastError();
 }
 
