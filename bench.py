@@ -222,6 +222,51 @@ def cpu_baseline(c, g, budget_s=10.0):
             "kind": "oracle", "sample": f"{what}; {n} passes in {el:.1f} s"}
 
 
+def graph_time(fns, calls=32, reps=5):
+    """Mean device time per call (us) of the calls fns[i % len(fns)], replayed
+    as one CUDA graph of `calls` calls."""
+    import torch
+    for fn in fns:
+        fn()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for i in range(calls):
+            fns[i % len(fns)]()
+    gr.replay()
+    gr.replay()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        gr.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+
+def time_decode_workload(name, dev, ops):
+    """(us per call, algorithmic bytes, plan) of one decode workload, inputs
+    rotated over enough copies to exceed 3x L2."""
+    import torch
+    d0 = device_decode_inputs(name, dev)
+    S, H, D = d0["q"].shape
+    Hk, B = d0["kc"].shape[2], d0["kc"].shape[1]
+    ncopy = max(1, min(8, math.ceil(3 * L2_BYTES / d0["bytes"])))
+    sets = [d0] + [dict(d0, q=d0["q"].clone(), kc=d0["kc"].clone(), vc=d0["vc"].clone(),
+                        out=torch.empty_like(d0["out"])) for _ in range(ncopy - 1)]
+    plan = ops.decode_plan(S, H, Hk, D, B, d0["max_ctx"])
+    work = torch.empty(max(plan[3], 256), dtype=torch.uint8, device=dev)
+    fns = [lambda d=d: ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"],
+                                                  d["cl"], d["max_ctx"], d["scale"],
+                                                  workspace=work) for d in sets]
+    us = graph_time(fns)
+    nbytes = d0["bytes"]
+    del d0, sets, work, fns
+    torch.cuda.empty_cache()
+    return us, nbytes, plan, ncopy
+
+
 def device_decode_inputs(name, dev):
     """Device inputs of a decode workload from a seeded torch generator (for
     timing and profiling: the kernels' speed does not depend on the values)."""
@@ -311,49 +356,13 @@ def run_sweep(args, local):
     if os.path.exists(pk_path):
         with open(pk_path) as f:
             peak = float(json.load(f).get("hbm_gbs") or peak)
-    calls = 32
-
-    def graph_time(fns):
-        """Mean device time per call of the given call list, replayed as a graph."""
-        for fn in fns:
-            fn()
-        torch.cuda.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            for i in range(calls):
-                fns[i % len(fns)]()
-        gr.replay()
-        gr.replay()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(5):
-            gr.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / (5 * calls)
-
     for name in decode_configs():
-        d0 = device_decode_inputs(name, dev)
-        S, H, D = d0["q"].shape
-        Hk, B = d0["kc"].shape[2], d0["kc"].shape[1]
-        ncopy = max(1, min(8, math.ceil(3 * L2_BYTES / d0["bytes"])))
-        sets = [d0] + [dict(d0, q=d0["q"].clone(), kc=d0["kc"].clone(), vc=d0["vc"].clone(),
-                            out=torch.empty_like(d0["out"])) for _ in range(ncopy - 1)]
-        ps, npart, path, ws = ops.decode_plan(S, H, Hk, D, B, d0["max_ctx"])
-        work = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
-        fns = [lambda d=d: ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"],
-                                                      d["cl"], d["max_ctx"], d["scale"],
-                                                      workspace=work) for d in sets]
-        us = graph_time(fns)
+        us, nbytes, (ps, npart, path, _), ncopy = time_decode_workload(name, dev, ops)
         print(json.dumps({"workload": name, "kind": "decode", "us_per_call": round(us, 2),
-                          "GBps": round(d0["bytes"] / us / 1e3, 1),
-                          "frac": round(d0["bytes"] / us / 1e3 / peak, 3),
+                          "GBps": round(nbytes / us / 1e3, 1),
+                          "frac": round(nbytes / us / 1e3 / peak, 3),
                           "path": "tc" if path == 1 else "simt", "partitions": npart,
-                          "partition_size": ps, "bytes": d0["bytes"], "copies": ncopy}),
-              flush=True)
-        del d0, sets, work, fns
-        torch.cuda.empty_cache()
+                          "partition_size": ps, "bytes": nbytes, "copies": ncopy}), flush=True)
     for name, cfg in gather_sweep().items():
         g = make_gather_case(name=name, **cfg)
         up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
@@ -552,52 +561,16 @@ def main():
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
 
-    # Large-batch GQA lines (decode alone), inputs generated on the device
-    # from a seeded torch generator; timing does not depend on the values.
+    # Large-batch GQA lines (decode alone): inputs from a seeded torch
+    # generator on the device (timing does not depend on the values), CUDA
+    # graph replays over rotated copies, as in the timed region above.
     targets = {}
     if not args.no_targets:
-        gen = torch.Generator(device=dev)
         for name in TARGETS:
-            cfg = decode_configs()[name]
-            gen.manual_seed(cfg["seed"])
-            Sx, Hx, Hkx, Dx, Bx = (cfg["num_seqs"], cfg["num_heads"], cfg["num_kv_heads"],
-                                   cfg["head_size"], cfg["block_size"])
-            Lx = cfg["context_lens"][0]
-            nbx = Sx * Lx // Bx
-            bf = torch.bfloat16
-            kcx = torch.randn((nbx, Bx, Hkx, Dx), generator=gen, device=dev, dtype=bf)
-            vcx = torch.randn((nbx, Bx, Hkx, Dx), generator=gen, device=dev, dtype=bf)
-            qx = torch.randn((Sx, Hx, Dx), generator=gen, device=dev, dtype=bf)
-            perm = torch.randperm(nbx, generator=gen, device=dev).to(torch.int32)
-            btx = perm.view(Sx, Lx // Bx).contiguous()
-            clx = torch.full((Sx,), Lx, dtype=torch.int32, device=dev)
-            outx = torch.empty_like(qx)
-            _, npx, pathx, wsx = ops.decode_plan(Sx, Hx, Hkx, Dx, Bx, Lx)
-            workx = torch.empty(max(wsx, 256), dtype=torch.uint8, device=dev)
-            scale = 1.0 / math.sqrt(Dx)
-            nbytes = Sx * Lx * Hkx * Dx * 2 * 2 + 2 * Sx * Hx * Dx * 2 + 4 * Sx * (Lx // Bx) + 4 * Sx
-            flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-
-            def call():
-                ops.paged_decode_attention(outx, qx, kcx, vcx, btx, clx, Lx, scale,
-                                           workspace=workx, stream=stream)
-            for _ in range(3):
-                call()
-            times = []
-            for _ in range(20):
-                flush.fill_(1)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                call()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                times.append(e0.elapsed_time(e1) * 1e3)
-            us = statistics.median(times)
+            us, nbytes, (ps, npx, pathx, _), ncopy = time_decode_workload(name, dev, ops)
             targets[name] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
-                             "path": "tc" if pathx == 1 else "simt", "partitions": npx}
-            del kcx, vcx, flush
-            torch.cuda.empty_cache()
+                             "path": "tc" if pathx == 1 else "simt", "partitions": npx,
+                             "copies": ncopy}
 
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peak, peak_src = FALLBACK_HBM_GBS, "fallback"

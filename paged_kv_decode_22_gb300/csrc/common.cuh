@@ -33,6 +33,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// Programmatic dependent launch.  Every kernel is launched so that the next
+// kernel in the stream may start while its CTAs drain; each kernel therefore
+// waits, before its first global-memory access, until the previous grid has
+// completed and its writes are visible, and then lets its own dependents
+// launch.  Without the launch attribute both instructions do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
 }

@@ -36,6 +36,8 @@ __device__ __forceinline__ void copy_row(char* dst, const char* src, int n16) {
 }
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(const CopyArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const bool is_v = blockIdx.y != 0;
   const size_t row_bytes = (size_t)a.row_elems * 2;
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const CopyArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) scatter_kernel(const CopyArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const bool is_v = blockIdx.y != 0;
   const size_t row_bytes = (size_t)a.row_elems * 2;
@@ -71,13 +75,11 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const CopyArgs a) {
 }  // namespace
 
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st) {
-  gather_kernel<<<dim3(a.num_tokens, 2), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3(a.num_tokens, 2), dim3(kThreads), 0, st, a);
 }
 
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st) {
-  scatter_kernel<<<dim3(a.num_tokens, 2), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(scatter_kernel, dim3(a.num_tokens, 2), dim3(kThreads), 0, st, a);
 }
 
 }  // namespace pkd

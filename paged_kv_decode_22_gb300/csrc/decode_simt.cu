@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(kThreads)
       for (int i = 0; i < kStages; ++i) mbar_init(&full[w][i], 1);
     fence_barrier_init();
   }
+  pdl_wait();
+  pdl_launch_dependents();
   // ---- entry: length, block ids of this partition (first pass) and q together
   const int L = a.context_lens[s];
   const int tab_tokens = a.max_blocks_per_seq << lb;
@@ -353,8 +355,8 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& km, const CUtensorM
   }
   const int g = a.num_heads / a.num_kv_heads;
   dim3 grid(a.num_partitions, a.num_kv_heads * (g / GC), a.num_seqs);
-  decode_simt_kernel<BF16, D, GC><<<grid, kThreads, Ring<D>::bytes, st>>>(km, vm, a);
-  return cudaGetLastError();
+  return launch_pdl(decode_simt_kernel<BF16, D, GC>, grid, dim3(kThreads), Ring<D>::bytes, st,
+                    km, vm, a);
 }
 
 template <bool BF16, int D>

@@ -323,6 +323,8 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     tmem_alloc(&ms.tmem_base, tmem_cols(NPAD));
     tmem_relinquish();
   }
+  pdl_wait();
+  pdl_launch_dependents();
   // Schedule: per-sequence unit counts, then an exclusive prefix sum by warp 0.
   if (a.num_seqs <= kSchedMax) {
     for (int i = threadIdx.x; i < a.num_seqs; i += kThreads) {
@@ -766,8 +768,8 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   const int grid = (int)(units < sms ? units : sms);
-  decode_tc_kernel<BF16, NPAD><<<grid, threads_of(NPAD), smem, st>>>(km, vm, qm, a);
-  return cudaGetLastError();
+  return launch_pdl(decode_tc_kernel<BF16, NPAD>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
+                    km, vm, qm, a);
 }
 
 template <bool BF16>

@@ -24,6 +24,8 @@ constexpr int kWarps = 4;
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(const DecodeArgs a) {
   constexpr int E = D / 32;  // elements per lane (2 or 4)
+  pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.num_heads;
   const long long sh = (long long)blockIdx.x * kWarps + warp;
@@ -82,8 +84,7 @@ template <bool BF16, int D>
 cudaError_t launch_r(const DecodeArgs& a, cudaStream_t st) {
   const long long rows = (long long)a.num_seqs * a.num_heads;
   const unsigned blocks = (unsigned)((rows + kWarps - 1) / kWarps);
-  lse_reduce_kernel<BF16, D><<<blocks, kWarps * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(lse_reduce_kernel<BF16, D>, dim3(blocks), dim3(kWarps * 32), 0, st, a);
 }
 
 }  // namespace
