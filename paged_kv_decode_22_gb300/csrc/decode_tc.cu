@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "schedule.cuh"
 #include "sm100.cuh"
 
 namespace pkd {
@@ -82,95 +83,10 @@ struct Misc {
   float lsum[4][64];            // per-warp exponent sums at finalisation
   alignas(16) float inv_l[64];       // 1 / sum (0 for a bad unit)
   float sum_l[64];                   // sum written to the workspace
-  // Schedule (sequences <= kSchedMax): lengths and the prefix count of work
-  // units (KV head x non-empty partition) of the sequences before s.
-  int sched_total;
-  int sched_L[1024];
-  int sched_pre[1025];
+  SchedSmem sched;                   // work-unit schedule
 };
-constexpr int kSchedMax = 1024;
 
 static_assert(sizeof(Misc) <= SmemLayout<16>::misc_bytes, "misc area too small");
-
-struct UnitInfo {
-  int s, hk, p, L, t0, t1, ntiles;
-  bool lok;
-};
-
-__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
-  UnitInfo ui;
-  const int P = a.num_partitions;
-  ui.p = u % P;
-  const int sh = u / P;
-  ui.hk = sh % a.num_kv_heads;
-  ui.s = sh / a.num_kv_heads;
-  ui.L = a.context_lens[ui.s];
-  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
-  ui.t0 = ui.p * a.partition_size;
-  ui.t1 = min(ui.t0 + a.partition_size, ui.L);
-  ui.ntiles = (ui.lok && ui.t0 < ui.L) ? (ui.t1 - ui.t0 + TT - 1) / TT : 0;
-  return ui;
-}
-
-__device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
-  return (len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && L > 0)
-             ? (L + a.partition_size - 1) / a.partition_size
-             : 0;
-}
-
-// The units one CTA processes, in order.  With at most kSchedMax sequences the
-// non-empty units are numbered densely (sequence, then KV head, then
-// partition) and each CTA takes an equal contiguous range; otherwise CTAs
-// take units round-robin and skip the empty ones.  Every role of a CTA walks
-// its own copy of the same cursor.
-struct UnitCursor {
-  long long next, end;
-  bool dense;
-};
-
-__device__ __forceinline__ UnitCursor cursor_begin(const Misc& ms, const DecodeArgs& a) {
-  UnitCursor c;
-  c.dense = a.num_seqs <= kSchedMax;
-  if (c.dense) {
-    const long long total = ms.sched_total;
-    c.next = total * blockIdx.x / gridDim.x;
-    c.end = total * (blockIdx.x + 1) / gridDim.x;
-  } else {
-    c.next = blockIdx.x;
-    c.end = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
-  }
-  return c;
-}
-
-__device__ __forceinline__ bool cursor_next(UnitCursor& c, const Misc& ms, const DecodeArgs& a,
-                                            UnitInfo& ui) {
-  if (c.dense) {
-    if (c.next >= c.end) return false;
-    const int j = (int)c.next++;
-    int lo = 0, hi = a.num_seqs - 1;   // last s with sched_pre[s] <= j
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ms.sched_pre[mid] <= j) lo = mid; else hi = mid - 1;
-    }
-    ui.s = lo;
-    ui.L = ms.sched_L[lo];
-    const int np = parts_of(a, ui.L);
-    const int r = j - ms.sched_pre[lo];
-    ui.hk = r / np;
-    ui.p = r - ui.hk * np;
-    ui.lok = true;
-    ui.t0 = ui.p * a.partition_size;
-    ui.t1 = min(ui.t0 + a.partition_size, ui.L);
-    ui.ntiles = (ui.t1 - ui.t0 + TT - 1) / TT;
-    return true;
-  }
-  while (c.next < c.end) {
-    ui = unit_info(a, (int)c.next);
-    c.next += gridDim.x;
-    if (ui.ntiles) return true;
-  }
-  return false;
-}
 
 __device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
   ms.abort = 1;
@@ -325,45 +241,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   }
   pdl_wait();
   pdl_launch_dependents();
-  // Schedule: per-sequence unit counts, then an exclusive prefix sum by warp 0.
-  if (a.num_seqs <= kSchedMax) {
-    for (int i = threadIdx.x; i < a.num_seqs; i += kThreads) {
-      const int L = a.context_lens[i];
-      ms.sched_L[i] = L;
-      ms.sched_pre[i + 1] = parts_of(a, L) * a.num_kv_heads;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int carry = 0;
-      for (int base = 0; base < a.num_seqs; base += 32) {
-        int v = base + lane < a.num_seqs ? ms.sched_pre[base + lane + 1] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, v, o);
-          if (lane >= o) v += n;
-        }
-        if (base + lane < a.num_seqs) ms.sched_pre[base + lane + 1] = v + carry;
-        carry += __shfl_sync(0xffffffffu, v, 31);
-      }
-      if (lane == 0) {
-        ms.sched_pre[0] = 0;
-        ms.sched_total = carry;
-      }
-    }
-  }
-  // Sequences with nothing to attend to: zero rows (unsplit; the merge writes
-  // them when split) and the length status bit.
-  for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
-    const int L = a.context_lens[sq];
-    if (parts_of(a, L) == 0) {
-      if (!len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && threadIdx.x == 0)
-        flag(a.status, PKD_DEV_BAD_LEN);
-      if (a.num_partitions == 1) {
-        uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)sq * a.num_heads * HD / 2;
-        for (int i = threadIdx.x; i < a.num_heads * HD / 2; i += kThreads) o[i] = 0u;
-      }
-    }
-  }
+  schedule_setup(ms.sched, a, kThreads);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -398,9 +276,9 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       }
       return raw;
     };
-    UnitCursor cur = cursor_begin(ms, a);
+    UnitCursor cur = cursor_begin(ms.sched, a);
     UnitInfo ui;
-    bool have = cursor_next(cur, ms, a, ui);
+    bool have = cursor_next<TT>(cur, ms.sched, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -410,7 +288,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       bool nhave = true;
       int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nhave = cursor_next(cur, ms, a, nui);
+        nhave = cursor_next<TT>(cur, ms.sched, a, nui);
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
@@ -486,9 +364,9 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         mma_commit(&ms.o_full[b]);
         mma_commit(&ms.v_empty[vs]);
       };
-      UnitCursor cur = cursor_begin(ms, a);
+      UnitCursor cur = cursor_begin(ms.sched, a);
       UnitInfo ui;
-      while (ok && cursor_next(cur, ms, a, ui)) {
+      while (ok && cursor_next<TT>(cur, ms.sched, a, ui)) {
         // The softmax warps finish the previous unit only after its last P V:
         // issue that one before this unit's first S.
         if (prev >= 0) {
@@ -572,9 +450,9 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       tc_fence_before();
     };
 
-    UnitCursor cur = cursor_begin(ms, a);
+    UnitCursor cur = cursor_begin(ms.sched, a);
     UnitInfo ui;
-    while (ok && cursor_next(cur, ms, a, ui)) {
+    while (ok && cursor_next<TT>(cur, ms.sched, a, ui)) {
       const int h0 = ui.hk * g;
       bool unit_bad = false;
       // Every wait below is bounded; a thread that gives up keeps taking part

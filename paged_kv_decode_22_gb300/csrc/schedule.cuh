@@ -1,0 +1,148 @@
+// Work units of the persistent decode kernels and their schedule.
+//
+// A unit is (sequence s, KV head, context partition p): the tokens
+// [p * partition_size, min((p + 1) * partition_size, L_s)) of one KV head,
+// processed in tiles of TT tokens.  With at most kSchedMax sequences every
+// CTA builds, in shared memory, the per-sequence count of non-empty units
+// and their prefix sum, numbers the non-empty units densely (sequence, then
+// KV head, then partition) and takes an equal contiguous range of them, so
+// empty partitions of short sequences cost nothing and the load is even.
+// With more sequences CTAs take units round-robin and skip the empty ones.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkd {
+
+constexpr int kSchedMax = 1024;
+
+struct SchedSmem {
+  int total;
+  int L[kSchedMax];        // context length of each sequence
+  int pre[kSchedMax + 1];  // units of the sequences before s
+};
+
+struct UnitInfo {
+  int s, hk, p, L, t0, t1, ntiles;
+  bool lok;
+};
+
+__device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
+  return (len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && L > 0)
+             ? (L + a.partition_size - 1) / a.partition_size
+             : 0;
+}
+
+template <int TT>
+__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
+  UnitInfo ui;
+  const int P = a.num_partitions;
+  ui.p = u % P;
+  const int sh = u / P;
+  ui.hk = sh % a.num_kv_heads;
+  ui.s = sh / a.num_kv_heads;
+  ui.L = a.context_lens[ui.s];
+  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
+  ui.t0 = ui.p * a.partition_size;
+  ui.t1 = min(ui.t0 + a.partition_size, ui.L);
+  ui.ntiles = (ui.lok && ui.t0 < ui.L) ? (ui.t1 - ui.t0 + TT - 1) / TT : 0;
+  return ui;
+}
+
+struct UnitCursor {
+  long long next, end;
+  bool dense;
+};
+
+__device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
+  UnitCursor c;
+  c.dense = a.num_seqs <= kSchedMax;
+  if (c.dense) {
+    const long long total = sc.total;
+    c.next = total * blockIdx.x / gridDim.x;
+    c.end = total * (blockIdx.x + 1) / gridDim.x;
+  } else {
+    c.next = blockIdx.x;
+    c.end = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  }
+  return c;
+}
+
+template <int TT>
+__device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
+                                            const DecodeArgs& a, UnitInfo& ui) {
+  if (c.dense) {
+    if (c.next >= c.end) return false;
+    const int j = (int)c.next++;
+    int lo = 0, hi = a.num_seqs - 1;   // last s with pre[s] <= j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sc.pre[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    ui.s = lo;
+    ui.L = sc.L[lo];
+    const int np = parts_of(a, ui.L);
+    const int r = j - sc.pre[lo];
+    ui.hk = r / np;
+    ui.p = r - ui.hk * np;
+    ui.lok = true;
+    ui.t0 = ui.p * a.partition_size;
+    ui.t1 = min(ui.t0 + a.partition_size, ui.L);
+    ui.ntiles = (ui.t1 - ui.t0 + TT - 1) / TT;
+    return true;
+  }
+  while (c.next < c.end) {
+    ui = unit_info<TT>(a, (int)c.next);
+    c.next += gridDim.x;
+    if (ui.ntiles) return true;
+  }
+  return false;
+}
+
+// Build the schedule (when dense) and zero the output rows of sequences that
+// have nothing to attend to (unsplit plans; the merge writes them when
+// split), setting the length status bit for invalid lengths.  Every thread
+// of the CTA calls this; it ends with __syncthreads().
+__device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& a, int nthreads) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (a.num_seqs <= kSchedMax) {
+    for (int i = threadIdx.x; i < a.num_seqs; i += nthreads) {
+      const int L = a.context_lens[i];
+      sc.L[i] = L;
+      sc.pre[i + 1] = parts_of(a, L) * a.num_kv_heads;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base < a.num_seqs; base += 32) {
+        int v = base + lane < a.num_seqs ? sc.pre[base + lane + 1] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += n;
+        }
+        if (base + lane < a.num_seqs) sc.pre[base + lane + 1] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) {
+        sc.pre[0] = 0;
+        sc.total = carry;
+      }
+    }
+  }
+  for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
+    const int L = a.context_lens[sq];
+    if (parts_of(a, L) == 0) {
+      if (!len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && threadIdx.x == 0)
+        flag(a.status, PKD_DEV_BAD_LEN);
+      if (a.num_partitions == 1) {
+        uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)sq * a.num_heads * a.head_size / 2;
+        for (int i = threadIdx.x; i < a.num_heads * a.head_size / 2; i += nthreads) o[i] = 0u;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace pkd
