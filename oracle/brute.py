@@ -9,8 +9,9 @@ from __future__ import annotations
 import math
 
 
-def dense_decode_attention(q, K, V, scale):
-    """q: [D] floats; K, V: [L][D] floats; returns [D] floats (zeros if L == 0)."""
+def dense_decode_attention(q, K, V, scale, alibi_slope=0.0):
+    """q: [D] floats; K, V: [L][D] floats; returns [D] floats (zeros if L == 0).
+    alibi_slope adds slope * (t - L + 1) to the logit of token t."""
     D = len(q)
     L = len(K)
     if L == 0:
@@ -20,7 +21,7 @@ def dense_decode_attention(q, K, V, scale):
         acc = 0.0
         for d in range(D):
             acc += q[d] * K[t][d]
-        logits.append(scale * acc)
+        logits.append(scale * acc + alibi_slope * (t - (L - 1)))
     top = max(logits)
     weights = [math.exp(x - top) for x in logits]
     total = math.fsum(weights)

@@ -21,6 +21,14 @@ after asserting ``num_heads % num_kv_heads == 0``, i.e. contiguous groups of
 query heads share one KV head.  num_kv_heads == num_heads is MHA, 1 is MQA,
 anything between is GQA.
 
+ALiBi (optional): "Optimize MQA Kernel" notes that MQA combines with ALiBi
+embeddings, and the kernel-latency runs of "[Performance] Support MQA/GQA in
+decode phase by using FlashAttention" are made with use_alibi=False.  The
+plain reading of ALiBi for the single decode query (position L - 1) adds a
+per-head linear bias to each logit:
+
+    logit[s, h, t] = scale * q . K_s[t] + slopes[h] * (t - L + 1)
+
 Readings of what the pages leave open (also listed in the design notes):
   * context_lens[s] == 0 gives an all-zero output row;
   * a sequence whose length is negative, exceeds the table
@@ -66,20 +74,31 @@ def gather_sequence_kv(cache_bits, block_tables, s: int, L: int, kv: int, dtype:
     return decode_bits(cache_bits[phys, t % B, kv, :], dtype)
 
 
-def attend(Q, K, V, scale: float):
-    """softmax over tokens of scale * Q K^T, times V.  Q [n, D], K/V [L, D] -> [n, D]."""
+def attend(Q, K, V, scale: float, bias=None):
+    """softmax over tokens of scale * Q K^T (+ bias [n, L]), times V.
+    Q [n, D], K/V [L, D] -> [n, D]."""
     X = float(scale) * (Q @ K.T)                          # [n, L]
+    if bias is not None:
+        X = X + bias
     X = X - X.max(axis=1, keepdims=True)
     P = np.exp(X)
     return (P @ V) / P.sum(axis=1, keepdims=True)
 
 
+def alibi_bias(slopes, heads, L: int):
+    """Bias [len(heads), L] = slopes[h] * (t - L + 1)."""
+    t = np.arange(L, dtype=np.float64) - (L - 1)
+    return np.asarray(slopes, dtype=np.float64)[list(heads)][:, None] * t[None, :]
+
+
 def paged_decode_attention(q, key_cache, value_cache, block_tables, context_lens, scale: float,
-                           dtype: str, *, pairs=None, max_context_len: int | None = None):
+                           dtype: str, *, pairs=None, max_context_len: int | None = None,
+                           alibi_slopes=None):
     """Reference decode attention.
 
     q: uint16 bits [S, H, D]; key_cache / value_cache: uint16 bits
     [NB, B, Hk, D]; block_tables: int [S, MB]; context_lens: int [S].
+    alibi_slopes: optional float [H] ALiBi slopes.
     Returns float64 [S, H, D], or [len(pairs), D] for a list of (s, h) pairs.
     """
     S, H, D = q.shape
@@ -107,7 +126,8 @@ def paged_decode_attention(q, key_cache, value_cache, block_tables, context_lens
                 continue
             K = gather_sequence_kv(key_cache, block_tables, s, L, kv, dtype)
             V = gather_sequence_kv(value_cache, block_tables, s, L, kv, dtype)
-            O = attend(decode_bits(q[s, hs, :], dtype), K, V, scale)
+            bias = None if alibi_slopes is None else alibi_bias(alibi_slopes, hs, L)
+            O = attend(decode_bits(q[s, hs, :], dtype), K, V, scale, bias)
             for i, h in enumerate(hs):
                 res[(s, h)] = O[i]
     if pairs is None:

@@ -90,6 +90,38 @@ def test_hand_case_kv_head_mapping_is_contiguous():
     assert [kv_head_of(h, 64, 8) for h in (0, 7, 8, 63)] == [0, 0, 1, 7]
 
 
+def test_hand_alibi_golden():
+    with open(os.path.join(GOLDEN, "hand_alibi.json")) as f:
+        g = json.load(f)
+    nan = float("nan")
+
+    def arr(v):
+        def fill(x):
+            if x is None:
+                return nan
+            if isinstance(x, list):
+                return [fill(y) for y in x]
+            return x
+        return np.array(fill(v), dtype=np.float32)
+
+    slopes = [math.log(2.0) if v == "ln2" else v for v in g["alibi_slopes"]]
+    out = paged_decode_attention(_bits(arr(g["q"]), "fp16"), _bits(arr(g["key_cache"]), "fp16"),
+                                 _bits(arr(g["value_cache"]), "fp16"),
+                                 np.array(g["block_tables"], np.int32),
+                                 np.array(g["context_lens"], np.int32), g["scale"], "fp16",
+                                 alibi_slopes=slopes)
+    np.testing.assert_allclose(out, np.array(g["expected_out"]), rtol=0, atol=1e-14)
+
+
+def test_alibi_with_zero_slopes_is_plain_attention():
+    c = _case(lens=(6, 21), H=6, Hk=2, D=8)
+    base = paged_decode_attention(c.q, c.key_cache, c.value_cache, c.block_tables,
+                                  c.context_lens, c.scale, "fp16")
+    zero = paged_decode_attention(c.q, c.key_cache, c.value_cache, c.block_tables,
+                                  c.context_lens, c.scale, "fp16", alibi_slopes=np.zeros(6))
+    np.testing.assert_array_equal(base, zero)
+
+
 # ---------------------------------------------------------------- brute force
 
 def _contiguous_rows(cache, table, L, B, kv, dtype):
@@ -124,6 +156,24 @@ def test_oracle_matches_brute_force(seed, H, Hk, D, B, lens, dtype):
             ref = dense_decode_attention(qv, K, V, c.scale)
             np.testing.assert_allclose(out[s, h], ref, rtol=0, atol=1e-12)
     assert np.isfinite(out).all()  # poisoned (NaN) slots were never read
+
+
+@pytest.mark.parametrize("seed,H,Hk,lens", [(21, 4, 2, [5, 19]), (22, 8, 1, [33, 1, 12])])
+def test_oracle_with_alibi_matches_brute_force(seed, H, Hk, lens):
+    c = make_decode_case(seed=seed, num_seqs=len(lens), num_heads=H, num_kv_heads=Hk,
+                         head_size=16, block_size=8, num_blocks=16, context_lens=lens,
+                         dtype="bf16")
+    slopes = [2.0 ** (-8.0 * (h + 1) / H) for h in range(H)]
+    out = paged_decode_attention(c.q, c.key_cache, c.value_cache, c.block_tables,
+                                 c.context_lens, c.scale, "bf16", alibi_slopes=slopes)
+    g = H // Hk
+    for s, L in enumerate(lens):
+        for h in range(H):
+            K = _contiguous_rows(c.key_cache, c.block_tables[s], L, 8, h // g, "bf16")
+            V = _contiguous_rows(c.value_cache, c.block_tables[s], L, 8, h // g, "bf16")
+            qv = [float(v) for v in decode_bits(c.q[s, h], "bf16")]
+            ref = dense_decode_attention(qv, K, V, c.scale, slopes[h])
+            np.testing.assert_allclose(out[s, h], ref, rtol=0, atol=1e-12)
 
 
 def test_sampled_pairs_equal_full_output():
