@@ -133,6 +133,25 @@ PKD_API pkd_status pkd_paged_decode_attention(void* out, const void* q, const vo
                                       size_t workspace_bytes, uint32_t* device_status,
                                       void* stream);
 
+/*
+ * pkd_paged_decode_attention with an optional ALiBi bias.  Same arguments,
+ * plus alibi_slopes: NULL, or a device array [num_heads] of float slopes
+ * (4-byte aligned).  With slopes, the logit of token t of sequence s for
+ * query head h becomes
+ *     scale * q[s,h,:] . K_s[t,:] + alibi_slopes[h] * (t - context_lens[s] + 1),
+ * the linear position bias that "Optimize MQA Kernel" (vLLM pull request
+ * 452) names as combining with MQA; the FlashAttention pull request's
+ * kernel-latency runs use it switched off.  NULL gives exactly
+ * pkd_paged_decode_attention.
+ */
+PKD_API pkd_status pkd_paged_decode_attention_ex(
+    void* out, const void* q, const void* key_cache, const void* value_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_size,
+    int block_size, int num_blocks, float scale, const float* alibi_slopes, pkd_dtype dtype,
+    int partition_size, void* workspace, size_t workspace_bytes, uint32_t* device_status,
+    void* stream);
+
 /* Size of the scratch array built into the library for
  * pkd_paged_decode_attention_static_ws (16 MiB per GPU that loads it). */
 #define PKD_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)

@@ -28,6 +28,8 @@ _SIGS = {
                         [ctypes.POINTER(_c_size)]),
     "pkd_paged_decode_attention": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
                                    [_c_float, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
+    "pkd_paged_decode_attention_ex": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
+                                      [_c_float, _vp, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
     "pkd_paged_decode_attention_static_ws": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
                                              [_c_float, _c_int, _c_int, _vp, _vp]),
     "pkd_gather_cached_kv": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_vp, _vp]),
@@ -112,14 +114,19 @@ def decode_plan(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_co
 
 def paged_decode_attention(out, q, key_cache, value_cache, block_tables, context_lens,
                            max_context_len, scale, partition_size=0, workspace=None,
-                           device_status=None, stream=None):
-    """out[s, h] = softmax(scale * q[s, h] . K_s^T) V_s through the block table.
+                           device_status=None, stream=None, alibi_slopes=None):
+    """out[s, h] = softmax(scale * q[s, h] . K_s^T [+ ALiBi]) V_s through the block table.
 
     q/out [S, H, D]; key_cache/value_cache [NB, B, Hk, D]; block_tables int32
-    [S, MB]; context_lens int32 [S].  ``workspace`` (uint8 CUDA tensor) is
-    allocated here through torch when the plan needs one and none is given.
+    [S, MB]; context_lens int32 [S]; alibi_slopes: None or float32 [H].
+    ``workspace`` (uint8 CUDA tensor) is allocated here through torch when the
+    plan needs one and none is given.
     """
-    _dense(out, q, key_cache, value_cache, block_tables, context_lens, workspace, device_status)
+    _dense(out, q, key_cache, value_cache, block_tables, context_lens, workspace, device_status,
+           alibi_slopes)
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or
+                                     alibi_slopes.numel() != q.shape[1]):
+        raise TypeError("alibi_slopes must be float32 [num_heads]")
     S, H, D = q.shape
     NB, B, Hk, _ = key_cache.shape
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
@@ -127,13 +134,13 @@ def paged_decode_attention(out, q, key_cache, value_cache, block_tables, context
     ps, npart, _, ws_bytes = decode_plan(S, H, Hk, D, B, max_context_len, partition_size)
     if npart > 1 and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    st = lib().pkd_paged_decode_attention(
+    st = lib().pkd_paged_decode_attention_ex(
         _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(context_lens), max_context_len, S, H, Hk, D, B, NB,
-        float(scale), _dtype_code(q), partition_size, _ptr(workspace),
+        float(scale), _ptr(alibi_slopes), _dtype_code(q), partition_size, _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(device_status), _stream(stream))
-    _check("pkd_paged_decode_attention", st)
+    _check("pkd_paged_decode_attention_ex", st)
     return out
 
 

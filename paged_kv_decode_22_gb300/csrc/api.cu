@@ -163,8 +163,25 @@ pkd_status pkd_paged_decode_attention(void* out, const void* q, const void* key_
                                       int partition_size, void* workspace,
                                       size_t workspace_bytes, uint32_t* device_status,
                                       void* stream) {
+  return pkd_paged_decode_attention_ex(out, q, key_cache, value_cache, block_tables,
+                                       max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                       num_heads, num_kv_heads, head_size, block_size, num_blocks,
+                                       scale, nullptr, dtype, partition_size, workspace,
+                                       workspace_bytes, device_status, stream);
+}
+
+pkd_status pkd_paged_decode_attention_ex(void* out, const void* q, const void* key_cache,
+                                         const void* value_cache, const int32_t* block_tables,
+                                         int max_blocks_per_seq, const int32_t* context_lens,
+                                         int max_context_len, int num_seqs, int num_heads,
+                                         int num_kv_heads, int head_size, int block_size,
+                                         int num_blocks, float scale, const float* alibi_slopes,
+                                         pkd_dtype dtype, int partition_size, void* workspace,
+                                         size_t workspace_bytes, uint32_t* device_status,
+                                         void* stream) {
   if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
     return PKD_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(alibi_slopes) & 3u) != 0) return PKD_ERR_ALIGN;
   if (dtype != PKD_FP16 && dtype != PKD_BF16) return PKD_ERR_UNSUPPORTED;
   if (!pow2_in(block_size, 8, 256)) return PKD_ERR_UNSUPPORTED;
   if (num_blocks < 1 || max_blocks_per_seq < 1) return PKD_ERR_SHAPE;
@@ -197,6 +214,7 @@ pkd_status pkd_paged_decode_attention(void* out, const void* q, const void* key_
   a.block_size = block_size;
   a.num_blocks = num_blocks;
   a.scale = scale;
+  a.alibi = alibi_slopes;
   a.is_bf16 = dtype == PKD_BF16;
   a.partition_size = plan.partition_size;
   a.num_partitions = plan.num_partitions;

@@ -140,6 +140,11 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
 
+  // ALiBi: logit += slope_j * (t - L + 1), in the same log2 units as q.
+  float slope[GC];
+#pragma unroll
+  for (int j = 0; j < GC; ++j) slope[j] = a.alibi ? a.alibi[h0 + j] * kLog2e : 0.f;
+
   float m[GC], l[GC], acc[GC][8];
 #pragma unroll
   for (int j = 0; j < GC; ++j) {
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(kThreads)
       float mx = -INFINITY;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (!okr[u]) x[u] = -INFINITY;
+        x[u] = okr[u] ? fmaf(slope[j], (float)(tb + u * SUBS + sub - (L - 1)), x[u]) : -INFINITY;
         mx = fmaxf(mx, x[u]);
       }
 #pragma unroll

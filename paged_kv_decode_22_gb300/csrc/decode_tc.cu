@@ -82,6 +82,7 @@ struct Misc {
   alignas(16) float alpha[2][64];    // rescale factor of each tile parity
   float lsum[4][64];            // per-warp exponent sums at finalisation
   alignas(16) float inv_l[64];       // 1 / sum (0 for a bad unit)
+  alignas(16) float slope[64];       // ALiBi slopes of the unit's heads (log2 units)
   float sum_l[64];                   // sum written to the workspace
   SchedSmem sched;                   // work-unit schedule
 };
@@ -452,9 +453,14 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
 
     UnitCursor cur = cursor_begin(ms.sched, a);
     UnitInfo ui;
+    const bool alibi = a.alibi != nullptr;
     while (ok && cursor_next<TT>(cur, ms.sched, a, ui)) {
       const int h0 = ui.hk * g;
       bool unit_bad = false;
+      if (alibi) {
+        if (et < my_heads) ms.slope[hbase + et] = a.alibi[h0 + hbase + et] * kLog2e;
+        named_barrier(bar, kSoftmaxThreads);
+      }
       // Every wait below is bounded; a thread that gives up keeps taking part
       // in the group barriers, which AND the flag so the group stops together.
       for (int jl = 0; jl < ui.ntiles; ++jl, ++j) {
@@ -469,15 +475,25 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         // Tile maxima per head (logits kept in registers for the exponentials).
         const uint32_t s_addr = lane_addr + b * NPAD + hbase;
         float xs[HPG];
+        const float pos = (float)(ts + row - (ui.L - 1));   // ALiBi distance to the query
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           float x[CH];
           tmem_ld<CH>(s_addr + c * CH, x);
+          if (alibi) {
+            float sl[CH];
 #pragma unroll
-          for (int i = 0; i < CH; ++i) {
-            x[i] = valid ? x[i] * qscale : -INFINITY;
-            xs[c * CH + i] = x[i];
+            for (int i = 0; i < CH; i += 4)
+              *reinterpret_cast<float4*>(&sl[i]) =
+                  *reinterpret_cast<const float4*>(&ms.slope[hbase + c * CH + i]);
+#pragma unroll
+            for (int i = 0; i < CH; ++i) x[i] = valid ? fmaf(sl[i], pos, x[i] * qscale) : -INFINITY;
+          } else {
+#pragma unroll
+            for (int i = 0; i < CH; ++i) x[i] = valid ? x[i] * qscale : -INFINITY;
           }
+#pragma unroll
+          for (int i = 0; i < CH; ++i) xs[c * CH + i] = x[i];
           const float m = chunk_max<CH>(x, lane);
           if (chunk_writer<CH>(lane)) ms.red[b][wq][hbase + c * CH + chunk_index<CH>(lane)] = m;
         }

@@ -43,6 +43,7 @@ struct DecodeArgs {
   int block_size;
   int num_blocks;
   float scale;
+  const float* alibi;   // [num_heads] ALiBi slopes, or nullptr
   int is_bf16;
   int partition_size;   // tokens per partition (multiple of 64)
   int num_partitions;   // 1 = write `out` directly

@@ -59,6 +59,16 @@ def test_decode_rejects_bad_arguments_on_host(lib, kw, code):
     assert _decode(lib, **kw) == code
 
 
+def test_decode_ex_rejects_misaligned_alibi_slopes(lib):
+    st = lib.pkd_paged_decode_attention_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 64, 2, 8, 2, 128,
+                                           16, 16, 0.1, ctypes.c_void_p(0x10002), 1, 0, NULL, 0,
+                                           NULL, NULL)
+    assert st == 5
+    assert lib.pkd_paged_decode_attention_ex(NULL, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 64, 2, 8, 2,
+                                             128, 16, 16, 0.1, NULL, 1, 0, NULL, 0, NULL,
+                                             NULL) == 1
+
+
 def _copy(lib, fn, **kw):
     a = dict(d0=FAKE, d1=FAKE, s0=FAKE, s1=FAKE, slots=FAKE, T=4, H=40, D=128, B=8, NB=16,
              dtype=0, st=NULL, stream=NULL)

@@ -90,6 +90,38 @@ def test_ragged_lengths_and_edges(H, Hk, D, B, dtype, partition_size):
     assert (got[lens.index(0)] == 0).all()
 
 
+ALIBI = [(8, 8, 128, 16, "fp16"), (12, 4, 64, 32, "bf16"), (64, 8, 128, 16, "bf16"),
+         (48, 1, 128, 16, "fp16"), (32, 1, 128, 64, "bf16")]
+
+
+@pytest.mark.parametrize("H,Hk,D,B,dtype", ALIBI)
+@pytest.mark.parametrize("partition_size", [0, 128])
+def test_alibi_matches_oracle(H, Hk, D, B, dtype, partition_size):
+    from paged_kv_decode_22_gb300 import ops
+
+    from .gpu_util import down_bits
+    lens = [1, B + 1, 300, 127, 1000, 0]
+    c = _ragged(23, H, Hk, D, B, lens, dtype)
+    dc = DeviceCase(c)
+    slopes = np.array([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], np.float32)
+    out = torch.full(c.q.shape, float("nan"), dtype=dc.q.dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.paged_decode_attention(out, dc.q, dc.kc, dc.vc, dc.bt, dc.cl, c.max_context_len,
+                               c.scale, partition_size=partition_size, device_status=status,
+                               alibi_slopes=torch.from_numpy(slopes).cuda())
+    torch.cuda.synchronize()
+    got = decode_bits(down_bits(out), dtype)
+    ref = _oracle(c, alibi_slopes=slopes.astype(np.float64))
+    assert int(status.item()) == 0
+    assert_close(got, ref, f"alibi H{H}/{Hk} D{D} B{B} ps{partition_size}")
+    # Slopes of zero reproduce plain attention.
+    ops.paged_decode_attention(out, dc.q, dc.kc, dc.vc, dc.bt, dc.cl, c.max_context_len,
+                               c.scale, partition_size=partition_size,
+                               alibi_slopes=torch.zeros(H, dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert_close(decode_bits(down_bits(out), dtype), _oracle(c), "zero slopes")
+
+
 def test_single_token_returns_value_row_exactly():
     c = _ragged(3, 16, 2, 128, 16, [1, 1, 1], "bf16")
     got, _ = run_decode(DeviceCase(c))
