@@ -55,6 +55,23 @@ NCU_TRAFFIC = {
 }
 
 
+def max_over_ranks(ms, dist, device):
+    """Step time of the slowest rank (every rank gets it); `dist` is
+    torch.distributed or None for a single process."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(step_bytes, world, ms):
+    """Whole-job throughput: every rank processed step_bytes per step, timed
+    by the slowest rank (weak scaling: the per-GPU work is fixed)."""
+    return step_bytes * world / ms / 1e6
+
+
 def env_int(name, default):
     try:
         return int(os.environ.get(name, default))
@@ -516,10 +533,7 @@ def main():
     dec_ms = sum(evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(len(plan)))
     gat_ms = sum(evs[2 * j + 1].elapsed_time(evs[2 * j + 2]) for j in range(len(plan)))
     ms = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     dec_us = dec_ms * 1e3 / args.steps
     gat_us = gat_ms * 1e3 / args.steps
     del graphs, tail, plan
@@ -594,7 +608,7 @@ def main():
         dom, dom_bytes, dom_us, dom_src = "gather_cached_kv", gat_b, gat_us, ("paged_kv_decode_22_gb300/csrc/copy_kv.cu",)
     achieved = dom_bytes / dom_us / 1e3
     traffic = NCU_TRAFFIC.get(src_hash(*dom_src))
-    value = step_bytes * world / ms / 1e6
+    value = whole_job_gbps(step_bytes, world, ms)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
