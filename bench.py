@@ -40,6 +40,7 @@ WORKLOAD = "llama13b_mha_b8_ctx256 decode + gather_t2048"
 DECODE_CFG = "llama13b_mha_b8_ctx256"
 GATHER_CFG = "gather_t2048"
 TARGETS = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "gqa_ctx4096_b256"]
+PATH_NAMES = {0: "simt", 1: "tc", 2: "tc_cluster"}   # decode_plan's kernel family
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -378,7 +379,7 @@ def run_sweep(args, local):
         print(json.dumps({"workload": name, "kind": "decode", "us_per_call": round(us, 2),
                           "GBps": round(nbytes / us / 1e3, 1),
                           "frac": round(nbytes / us / 1e3 / peak, 3),
-                          "path": "tc" if path == 1 else "simt", "partitions": npart,
+                          "path": PATH_NAMES[path], "partitions": npart,
                           "partition_size": ps, "bytes": nbytes, "copies": ncopy}), flush=True)
     for name, cfg in gather_sweep().items():
         g = make_gather_case(name=name, **cfg)
@@ -583,7 +584,7 @@ def main():
         for name in TARGETS:
             us, nbytes, (ps, npx, pathx, _), ncopy = time_decode_workload(name, dev, ops)
             targets[name] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
-                             "path": "tc" if pathx == 1 else "simt", "partitions": npx,
+                             "path": PATH_NAMES[pathx], "partitions": npx,
                              "copies": ncopy}
 
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -617,7 +618,7 @@ def main():
         "config": {"workload": WORKLOAD, "decode": "S=8 H=40 Hk=40 D=128 B=16 ctx=256 NB=2048",
                    "gather": "T=2048 H=40 D=128 B=8 NB=1024",
                    "l2": f"inputs rotate over {ncopy} device copies (>3x L2 touched per cycle)",
-                   "decode_partitions": npart, "decode_path": "tc" if path == 1 else "simt"},
+                   "decode_partitions": npart, "decode_path": PATH_NAMES[path]},
         "decode_us_per_call": round(dec_us, 2), "gather_us_per_call": round(gat_us, 2),
         "step_bytes": step_bytes,
         "gpu_launches": launches_per_step * args.steps,

@@ -82,6 +82,8 @@ typedef enum pkd_dtype { PKD_FP16 = 0, PKD_BF16 = 1 } pkd_dtype;
 /* Decode kernel families, as reported by pkd_decode_plan(). */
 #define PKD_PATH_SIMT 0   /* CUDA-core path (query-group size below 4) */
 #define PKD_PATH_TC 1     /* tcgen05 tensor-core path with TMA staging */
+#define PKD_PATH_TC_CLUSTER 2 /* the same, its context partitions merged inside
+                                 thread-block clusters: no workspace, one launch */
 
 /*
  * Launch plan of pkd_paged_decode_attention for the given sizes on the
@@ -90,8 +92,12 @@ typedef enum pkd_dtype { PKD_FP16 = 0, PKD_BF16 = 1 } pkd_dtype;
  * that partition length.  Outputs
  * (any may be NULL): the partition length in tokens, the number of
  * partitions (1 = no split, no reduction launch), the kernel family, and the
- * workspace bytes the call needs (0 when unsplit).  Pure host arithmetic
- * plus a cached device-attribute query; allocates nothing.
+ * workspace bytes the call needs (0 when unsplit, and for
+ * PKD_PATH_TC_CLUSTER, whose split is merged inside the one launch).  The
+ * tensor-core path merges a split inside thread-block clusters when it has
+ * at most 16 partitions and the clusters of all (sequence, KV head) pairs fit
+ * on the device at once.  Pure host arithmetic plus cached device-attribute
+ * and occupancy queries; allocates nothing.
  */
 PKD_API pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                            int block_size, int max_context_len, int partition_size,
@@ -115,8 +121,8 @@ PKD_API pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads
  *   scale         logit multiplier (1/sqrt(head_size) for standard attention)
  *   partition_size  0 = library choice, else a multiple of 64 tokens
  *   workspace     device scratch of >= the plan's workspace bytes (may be
- *                 NULL when the plan has one partition); its contents on
- *                 entry do not matter and are clobbered
+ *                 NULL when that is 0); its contents on entry do not matter
+ *                 and are clobbered
  *   device_status optional device uint32_t for PKD_DEV_* bits
  * Results are rounded to nearest-even from fp32 accumulation.  A sequence
  * with context_lens[s] == 0 yields zeros.  A sequence with an invalid length

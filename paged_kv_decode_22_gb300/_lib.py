@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libpkd.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "pkd.h")
 
 FP16, BF16 = 0, 1
-PATH_SIMT, PATH_TC = 0, 1
+PATH_SIMT, PATH_TC, PATH_TC_CLUSTER = 0, 1, 2
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8
 
 _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
@@ -132,7 +132,7 @@ def paged_decode_attention(out, q, key_cache, value_cache, block_tables, context
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables and context_lens must be int32")
     ps, npart, _, ws_bytes = decode_plan(S, H, Hk, D, B, max_context_len, partition_size)
-    if npart > 1 and workspace is None:
+    if ws_bytes > 0 and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     st = lib().pkd_paged_decode_attention_ex(
         _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),

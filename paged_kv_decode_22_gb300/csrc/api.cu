@@ -53,10 +53,14 @@ bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1))
 constexpr int kPartitionQuantum = 64;   // partitions are whole 64-token tiles
 constexpr int kTargetCtasPerSm = 2;     // split until about this many CTAs per SM
 
+constexpr int kMaxCluster = 16;         // partitions merged inside one cluster, at most
+constexpr double kClusterMergeCost = 0.5;   // in-cluster merge, in tiles
+
 struct Plan {
   int partition_size = kPartitionQuantum;
   int num_partitions = 1;
   int path = PKD_PATH_SIMT;
+  bool fused = false;                   // tensor-core split merged inside clusters
   size_t ws_bytes = 0;
   size_t off_m = 0, off_l = 0;
 };
@@ -84,6 +88,19 @@ double tc_cost(long long units, int tiles, int P, int ctas) {
   return (double)per_cta * tiles_per_unit + 0.25 * per_cta + (P > 1 ? 2.0 : 0.0);
 }
 
+// A split into P partitions is merged inside thread-block clusters (one
+// cluster of P CTAs per (sequence, KV head), no workspace, no merge launch)
+// when all the clusters fit on the device at once.
+bool cluster_fits(long long units, int group, int P) {
+  if (P < 2 || P > kMaxCluster || units > 65535) return false;
+  const int cap = pkd::decode_tc_cluster_capacity(group, P);
+  return cap > 0 && units <= cap;
+}
+
+double tc_cluster_cost(int tiles, int P) {
+  return (double)((tiles + P - 1) / P) + 0.25 + kClusterMergeCost;
+}
+
 pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                      int max_context_len, int block_size, int partition_size, Plan* plan) {
   pkd_status st = check_decode_sizes(num_seqs, num_heads, num_kv_heads, head_size, max_context_len);
@@ -107,7 +124,8 @@ pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_siz
     int best = 1;
     double best_cost = tc_cost(units, max_tiles, 1, dev.sms);
     for (int P = 2; P <= max_tiles && P <= 64; ++P) {
-      const double c = tc_cost(units, max_tiles, P, dev.sms);
+      const double c = cluster_fits(units, g, P) ? tc_cluster_cost(max_tiles, P)
+                                                 : tc_cost(units, max_tiles, P, dev.sms);
       if (c < best_cost * 0.97) {
         best_cost = c;
         best = P;
@@ -124,7 +142,8 @@ pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_siz
   }
   p.num_partitions = std::max(1, (max_context_len + p.partition_size - 1) / p.partition_size);
   if (p.num_partitions > 65535) return PKD_ERR_SHAPE;
-  if (p.num_partitions > 1) {
+  p.fused = tc && cluster_fits((long long)num_seqs * num_kv_heads, g, p.num_partitions);
+  if (p.num_partitions > 1 && !p.fused) {
     const size_t rows = (size_t)num_seqs * num_heads * p.num_partitions;
     p.off_m = align256(rows * head_size * sizeof(float));
     p.off_l = p.off_m + align256(rows * sizeof(float));
@@ -149,7 +168,7 @@ pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int he
   if (st != PKD_OK) return st;
   if (out_partition_size) *out_partition_size = p.partition_size;
   if (out_num_partitions) *out_num_partitions = p.num_partitions;
-  if (out_path) *out_path = p.path;
+  if (out_path) *out_path = p.fused ? PKD_PATH_TC_CLUSTER : p.path;
   if (out_workspace_bytes) *out_workspace_bytes = p.ws_bytes;
   return PKD_OK;
 }
@@ -193,7 +212,7 @@ pkd_status pkd_paged_decode_attention_ex(void* out, const void* q, const void* k
   pkd_status st = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_context_len,
                             block_size, partition_size, &plan);
   if (st != PKD_OK) return st;
-  if (plan.num_partitions > 1) {
+  if (plan.ws_bytes > 0) {
     if (!workspace || workspace_bytes < plan.ws_bytes) return PKD_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKD_ERR_ALIGN;
   }
@@ -218,16 +237,18 @@ pkd_status pkd_paged_decode_attention_ex(void* out, const void* q, const void* k
   a.is_bf16 = dtype == PKD_BF16;
   a.partition_size = plan.partition_size;
   a.num_partitions = plan.num_partitions;
+  a.fused = plan.fused ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
-  a.ws_o = plan.num_partitions > 1 ? reinterpret_cast<float*>(ws) : nullptr;
-  a.ws_m = plan.num_partitions > 1 ? reinterpret_cast<float*>(ws + plan.off_m) : nullptr;
-  a.ws_l = plan.num_partitions > 1 ? reinterpret_cast<float*>(ws + plan.off_l) : nullptr;
+  const bool use_ws = plan.ws_bytes > 0;
+  a.ws_o = use_ws ? reinterpret_cast<float*>(ws) : nullptr;
+  a.ws_m = use_ws ? reinterpret_cast<float*>(ws + plan.off_m) : nullptr;
+  a.ws_l = use_ws ? reinterpret_cast<float*>(ws + plan.off_l) : nullptr;
   a.status = device_status;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = plan.path == PKD_PATH_TC ? pkd::launch_decode_tc(a, s) : pkd::launch_decode_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (plan.num_partitions > 1) {
+  if (use_ws) {
     e = pkd::launch_lse_reduce(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "lse_reduce launch");
   }

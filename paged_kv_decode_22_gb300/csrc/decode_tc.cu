@@ -46,6 +46,7 @@ constexpr int TILE_BYTES = TT * HD * 2; // one K or V tile, 32 KB
 constexpr int kSoftmaxThreads = 128;   // one softmax warpgroup
 constexpr int kNoBlock = -2147483647 - 1;  // "no block here" marker of the producers
 constexpr uint32_t kSoftmaxBar = 1;     // named barrier id of softmax group 0 (group 1: 2)
+constexpr int kMaxCluster = 16;         // partitions merged inside one cluster, at most
 
 __host__ __device__ constexpr int k_stages(int npad) { return npad <= 48 ? 3 : 2; }
 __host__ __device__ constexpr int v_stages(int npad) { return npad <= 16 ? 3 : 2; }
@@ -424,6 +425,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float qscale = a.scale * kLog2e;
     const bool single = a.num_partitions == 1;
+    const bool fused = a.fused != 0;           // one unit, merged over the cluster
     const int H = a.num_heads;
     const int my_heads = max(0, min(HPG, g - hbase));    // valid heads of this warpgroup
     float o_acc[HPG], l_part[HPG];
@@ -598,13 +600,14 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         for (int hl = 0; hl < HPG; ++hl) {
           if (hl < my_heads) reinterpret_cast<float*>(piece(hl / per))[(hl % per) * HD + row] = o_acc[hl];
         }
-        if (et < my_heads) {
+        if (et < my_heads && !fused) {
           a.ws_m[unit_row + hbase + et] = ms.m_run[hbase + et];
           a.ws_l[unit_row + hbase + et] = ms.sum_l[hbase + et];
         }
       }
       fence_proxy_async_smem();
       named_barrier(bar, kSoftmaxThreads);
+      if (fused) break;   // the cluster merge reads the staged partial
       if (leader) {
         const int per = single ? HPG / 2 : HPG / 4;
         const int esz = single ? 2 : 4;
@@ -632,11 +635,109 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols(NPAD));
   }
+
+  // ---------------------------------------------------------------- cluster merge
+  // Fused split context: the CTAs of the cluster are the partitions of one
+  // (sequence, KV head), and each has left its partial in shared memory: the
+  // unnormalised o rows (fp32, in its P buffers), the maxima m (log2 domain)
+  // and the sums l (negative for a bad block).  Heads are dealt round-robin
+  // to the ranks; a warp merges one head, each lane 4 columns of d:
+  //     M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
+  if (a.fused) {
+    cluster_sync();
+    constexpr int HPG = NPAD / GROUPS, PER = HPG / 4;   // staging: PER rows per piece
+    const int P = a.num_partitions;
+    const uint32_t rank = cluster_ctarank();
+    const int s = blockIdx.y / a.num_kv_heads;
+    const int hk = blockIdx.y - s * a.num_kv_heads;
+    const int L = a.context_lens[s];
+    const int np = parts_of(a, L);
+    if (rank == 0 && hk == 0 && threadIdx.x == 0 &&
+        !len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size))
+      flag(a.status, PKD_DEV_BAD_LEN);
+    for (int h = (int)rank + P * warp; h < g; h += P * (kThreads / 32)) {
+      const int grp = h / HPG, hl = h - grp * HPG, q = hl / PER;
+      const uint8_t* row = pbuf + (q >> 1) * LY::QB + (q & 1) * NPAD * 128 + grp * HPG * 128 +
+                           (hl - q * PER) * HD * 4 + lane * 16;
+      float m[kMaxCluster], l[kMaxCluster];
+      float M = -INFINITY;
+      bool bad = false;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < np) {
+          m[r] = ld_dsmem(dsmem_addr(&ms.m_run[h], r));
+          l[r] = ld_dsmem(dsmem_addr(&ms.sum_l[h], r));
+          M = fmaxf(M, m[r]);
+          bad |= l[r] < 0.f;
+        }
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
+      if (!bad && M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (r < np) {
+            const float w = exp2f(m[r] - M);
+            const float4 o = ld_dsmem4(dsmem_addr(row, r));
+            den = fmaf(w, l[r], den);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+          }
+        }
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      uint2 v;
+      v.x = pack2<BF16>(acc.x * inv, acc.y * inv);
+      v.y = pack2<BF16>(acc.z * inv, acc.w * inv);
+      const size_t orow = (size_t)s * a.num_heads + (size_t)hk * g + h;
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + orow * HD + lane * 4) = v;
+    }
+    cluster_sync();   // every rank's shared memory stays until all have read it
+  }
 }
 
 // ---------------------------------------------------------------- host side
 
 int pad_group(int g) { return (g + 15) / 16 * 16; }
+
+// Kernel attributes, set once per device: the dynamic shared memory and
+// clusters of up to 16 CTAs.
+template <bool BF16, int NPAD>
+cudaError_t prepare(int* smem_out) {
+  const int smem = SmemLayout<NPAD>::bytes + 1024;
+  *smem_out = smem;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || attr_set[dev]) return cudaSuccess;
+  if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return e;
+  attr_set[dev] = true;
+  return cudaSuccess;
+}
+
+void cluster_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&attr)[2], dim3 grid,
+                    int threads, int smem, int cluster, cudaStream_t st) {
+  *cfg = {};
+  cfg->gridDim = grid;
+  cfg->blockDim = dim3(threads);
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 2;
+}
 
 template <bool BF16, int NPAD>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
@@ -647,23 +748,47 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
       !make_kv_map(&vm, a.value_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
       !make_rows_map(&qm, a.q, BF16, HD, (long long)a.num_seqs * a.num_heads, 64, NPAD))
     return cudaErrorInvalidValue;
-
-  const int smem = SmemLayout<NPAD>::bytes + 1024;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+  int smem = 0;
+  cudaError_t e = prepare<BF16, NPAD>(&smem);
+  if (e != cudaSuccess) return e;
+  if (a.fused) {
+    // One cluster of P CTAs per (sequence, KV head).
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config(&cfg, attr, dim3(a.num_partitions, a.num_seqs * a.num_kv_heads),
+                   threads_of(NPAD), smem, a.num_partitions, st);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BF16, NPAD>, km, vm, qm, a);
   }
-  int sms = 0;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   const int grid = (int)(units < sms ? units : sms);
   return launch_pdl(decode_tc_kernel<BF16, NPAD>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
                     km, vm, qm, a);
+}
+
+// Co-resident clusters of `cluster` CTAs, cached per device and cluster size.
+template <int NPAD>
+int capacity_t(int cluster) {
+  static int cache[64][kMaxCluster + 1];   // value + 1; 0 = not yet queried
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int& c = cache[dev][cluster];
+  if (c == 0) {
+    int smem = 0, n = 0;
+    if (prepare<true, NPAD>(&smem) == cudaSuccess) {
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr[2];
+      cluster_config(&cfg, attr, dim3(cluster), threads_of(NPAD), smem, cluster, nullptr);
+      if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<true, NPAD>, &cfg) != cudaSuccess) {
+        cudaGetLastError();   // a refused query only means "no cluster launch"
+        n = 0;
+      }
+    }
+    c = n + 1;
+  }
+  return c - 1;
 }
 
 template <bool BF16>
@@ -684,6 +809,17 @@ bool decode_tc_supported(int head_size, int group, int block_size) {
 }
 
 int decode_tc_tile() { return TT; }
+
+int decode_tc_cluster_capacity(int group, int cluster) {
+  if (cluster < 2 || cluster > kMaxCluster || group < 4 || group > 64) return 0;
+  switch (pad_group(group)) {
+    case 16: return capacity_t<16>(cluster);
+    case 32: return capacity_t<32>(cluster);
+    case 48: return capacity_t<48>(cluster);
+    case 64: return capacity_t<64>(cluster);
+  }
+  return 0;
+}
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   return a.is_bf16 ? launch_b<true>(a, st) : launch_b<false>(a, st);

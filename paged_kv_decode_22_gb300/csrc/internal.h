@@ -47,6 +47,9 @@ struct DecodeArgs {
   int is_bf16;
   int partition_size;   // tokens per partition (multiple of 64)
   int num_partitions;   // 1 = write `out` directly
+  int fused;            // tensor-core path only: the partitions of one (sequence,
+                        // KV head) form one thread-block cluster and are merged
+                        // through distributed shared memory (no workspace)
   float* ws_o;          // [S][Hk][P][H/Hk][D] unnormalised partial outputs
   float* ws_m;          // [S][Hk][P][H/Hk] partial maxima (log2 domain)
   float* ws_l;          // [S][Hk][P][H/Hk] partial sums; < 0 marks a bad block
@@ -80,6 +83,9 @@ int simt_heads_per_cta(int group);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 bool decode_tc_supported(int head_size, int group, int block_size);
 int decode_tc_tile();
+// Clusters of `cluster` CTAs of the tensor-core kernel for query-group size
+// `group` that the current device holds at once (0: cannot launch).
+int decode_tc_cluster_capacity(int group, int cluster);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st);

@@ -57,8 +57,12 @@ struct UnitCursor {
 
 __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
   UnitCursor c;
-  c.dense = a.num_seqs <= kSchedMax;
-  if (c.dense) {
+  c.dense = !a.fused && a.num_seqs <= kSchedMax;
+  if (a.fused) {
+    // Cluster launch: grid (P, S * Hk), one unit per CTA, partition = x.
+    c.next = (long long)blockIdx.y * a.num_partitions + blockIdx.x;
+    c.end = c.next + 1;
+  } else if (c.dense) {
     const long long total = sc.total;
     c.next = total * blockIdx.x / gridDim.x;
     c.end = total * (blockIdx.x + 1) / gridDim.x;
@@ -106,6 +110,10 @@ __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
 // of the CTA calls this; it ends with __syncthreads().
 __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& a, int nthreads) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (a.fused) {   // one unit per CTA; the cluster merge handles empty sequences
+    __syncthreads();
+    return;
+  }
   if (a.num_seqs <= kSchedMax) {
     for (int i = threadIdx.x; i < a.num_seqs; i += nthreads) {
       const int L = a.context_lens[i];
