@@ -28,6 +28,14 @@
 //              final (or partial, for split context) result written.
 // Shared-memory operands use the 128-byte swizzled canonical layouts: K, q and
 // P K-major, V MN-major (head_size contiguous).
+//
+// Split context comes in two forms.  Workspace form: each unit writes its
+// partial (o, m, l) to global memory and lse_reduce merges them in a second
+// launch.  Cluster form (small grids): the P partitions of one (sequence, KV
+// head) are the P CTAs of one thread-block cluster, one unit each; they keep
+// their partials in shared memory and merge them over distributed shared
+// memory before the kernel ends, so there is neither workspace nor merge
+// launch.
 #include <cuda.h>
 
 #include "common.cuh"

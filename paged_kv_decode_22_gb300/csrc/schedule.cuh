@@ -8,6 +8,8 @@
 // KV head, then partition) and takes an equal contiguous range of them, so
 // empty partitions of short sequences cost nothing and the load is even.
 // With more sequences CTAs take units round-robin and skip the empty ones.
+// In the cluster form of the tensor-core kernel each CTA takes the single
+// unit its grid position names (x = partition, y = sequence * Hk + KV head).
 #pragma once
 
 #include "common.cuh"
