@@ -29,6 +29,16 @@
 // warp runs its own online softmax over the tokens it loads; the four warps
 // are merged through shared memory at the end.
 //
+// Arithmetic per 8-token box: q . k with mixed-precision FMAs (16-bit
+// operands, fp32 accumulation: exact products, no conversions); the per-lane
+// partial dots of a lane's rows are summed across the row's lanes by a
+// halving butterfly, after which each lane holds one row's logit, so one
+// exponential per lane covers the box; the running rescale runs only when
+// the maximum moves; p, rounded to the input's 16-bit type (as the
+// tensor-core path's P operand is), is broadcast to the lanes of its row and
+// accumulated into o with the same mixed-precision FMA.  l sums the unrounded
+// fp32 p.
+//
 // Output: with one partition the CTA writes `out` directly; otherwise it
 // writes the unnormalised partial (o, m, l) that lse_reduce.cu merges.
 #include <cuda.h>
@@ -54,6 +64,74 @@ struct Ring {
   static constexpr int stage = 2 * box;
   static constexpr int bytes = kWarps * kStages * stage + 128;   // + alignment slack
 };
+
+// Dot product of 8 16-bit elements of k and q with fp32 accumulation: each
+// product of two 16-bit values is exact in fp32, so the mixed-precision FMA
+// gives the same result as converting both operands first.
+template <bool BF16>
+__device__ __forceinline__ float dot8(const uint4& k, const uint4& q) {
+  float d = 0.f;
+  const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
+  const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF16)
+      asm("{\n\t.reg .b16 kl, kh, ql, qh;\n\t"
+          "mov.b32 {kl, kh}, %1;\n\tmov.b32 {ql, qh}, %2;\n\t"
+          "fma.rn.f32.bf16 %0, kl, ql, %0;\n\tfma.rn.f32.bf16 %0, kh, qh, %0;\n\t}"
+          : "+f"(d) : "r"(kk[i]), "r"(qq[i]));
+    else
+      asm("{\n\t.reg .b16 kl, kh, ql, qh;\n\t"
+          "mov.b32 {kl, kh}, %1;\n\tmov.b32 {ql, qh}, %2;\n\t"
+          "fma.rn.f32.f16 %0, kl, ql, %0;\n\tfma.rn.f32.f16 %0, kh, qh, %0;\n\t}"
+          : "+f"(d) : "r"(kk[i]), "r"(qq[i]));
+  }
+  return d;
+}
+
+// acc[i] += p * v[i] for 8 16-bit elements of v, p a 16-bit probability in
+// the low half of `p16` (the same rounding of p as the tensor-core path's P
+// operand), fp32 accumulation.
+template <bool BF16>
+__device__ __forceinline__ void axpy8(float (&acc)[8], uint32_t p16, const uint4& v) {
+  const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BF16)
+      asm("{\n\t.reg .b16 vl, vh, p, pz;\n\t"
+          "mov.b32 {vl, vh}, %2;\n\tmov.b32 {p, pz}, %3;\n\t"
+          "fma.rn.f32.bf16 %0, p, vl, %0;\n\tfma.rn.f32.bf16 %1, p, vh, %1;\n\t}"
+          : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1]) : "r"(vv[i]), "r"(p16));
+    else
+      asm("{\n\t.reg .b16 vl, vh, p, pz;\n\t"
+          "mov.b32 {vl, vh}, %2;\n\tmov.b32 {p, pz}, %3;\n\t"
+          "fma.rn.f32.f16 %0, p, vl, %0;\n\tfma.rn.f32.f16 %1, p, vh, %1;\n\t}"
+          : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1]) : "r"(vv[i]), "r"(p16));
+  }
+}
+
+// Sums over the TPG lanes of a token row of U per-lane partial dot products
+// (one per row u of the lane's sub-row), by a halving butterfly: each step
+// trades half of the remaining values with the partner lane.  Lane `part`
+// ends with the full sum of row u = part / (TPG / U).
+template <int TPG, int U>
+__device__ __forceinline__ float reduce_rows(const float (&d)[U], int part) {
+  if constexpr (U == 4) {
+    static_assert(TPG == 16, "U = 4 rows per lane goes with 16 lanes per row");
+    const bool b3 = part & 8, b2 = part & 4;
+    float w0 = (b3 ? d[2] : d[0]) + __shfl_xor_sync(0xffffffffu, b3 ? d[0] : d[2], 8);
+    float w1 = (b3 ? d[3] : d[1]) + __shfl_xor_sync(0xffffffffu, b3 ? d[1] : d[3], 8);
+    float w = (b2 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, b2 ? w0 : w1, 4);
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    return w + __shfl_xor_sync(0xffffffffu, w, 1);
+  } else {
+    static_assert(U == 2 && TPG == 8, "U = 2 rows per lane goes with 8 lanes per row");
+    const bool b2 = part & 4;
+    float w = (b2 ? d[1] : d[0]) + __shfl_xor_sync(0xffffffffu, b2 ? d[0] : d[1], 4);
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    return w + __shfl_xor_sync(0xffffffffu, w, 1);
+  }
+}
 
 template <bool BF16, int D, int GC>
 __global__ void __launch_bounds__(kThreads)
@@ -128,18 +206,6 @@ __global__ void __launch_bounds__(kThreads)
   }
   const int t1 = min(t0 + a.partition_size, L);
 
-  float qr[GC][8];
-#pragma unroll
-  for (int j = 0; j < GC; ++j) {
-    const uint32_t ww[4] = {qw[j].x, qw[j].y, qw[j].z, qw[j].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 f = unpack2<BF16>(ww[i]);
-      qr[j][2 * i] = f.x * qscale;
-      qr[j][2 * i + 1] = f.y * qscale;
-    }
-  }
-
   // ALiBi: logit += slope_j * (t - L + 1), in the same log2 units as q.
   float slope[GC];
 #pragma unroll
@@ -154,9 +220,6 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
   }
 
-  const size_t slot_stride = (size_t)a.num_kv_heads * D;  // elements per cache slot
-  const uint16_t* kbase = reinterpret_cast<const uint16_t*>(a.key_cache) + (size_t)hk * D + part * 8;
-  const uint16_t* vbase = reinterpret_cast<const uint16_t*>(a.value_cache) + (size_t)hk * D + part * 8;
   bool bad = false;
 
   // Blocks [pb0, pb0 + kMaxIds) of the partition have their ids in shared memory.
@@ -185,6 +248,12 @@ __global__ void __launch_bounds__(kThreads)
     ++wi_issue;
   };
 
+  // Row of the box whose logit this lane holds after the row reduction (see
+  // reduce_rows), and the lane holding row u's logit for this lane's sub-row.
+  constexpr int kRowLanes = TPG / U;                 // lanes that end with the same row
+  const int u_mine = part / kRowLanes;
+  const int r_mine = u_mine * SUBS + sub;
+
   auto consume = [&](int tb) {
     const int st = wi_use % kStages;
     ok_wait = __all_sync(0xffffffffu, ok_wait && mbar_wait(&full[warp][st], (wi_use / kStages) & 1));
@@ -192,63 +261,56 @@ __global__ void __launch_bounds__(kThreads)
     if (!ok_wait) return;
     const int id = ids[(tb >> lb) - pb0];
     const bool in_range = id >= 0 && id < a.num_blocks;
-    const uint8_t* src = wring + st * Ring<D>::stage;
-    float kf[U][8], vf[U][8];
-    bool okr[U];
+    // Rows [0, nvalid) of the box are attended (warp-uniform).  Boxes of bad
+    // ids were zero-filled by TMA; rows past the sequence end inside a good
+    // block may hold anything (NaN included), so their V is zeroed here.
+    const int nvalid = in_range ? min(kRows, t1 - tb) : 0;
+    uint8_t* src = wring + st * Ring<D>::stage;
+    if (in_range && nvalid < kRows) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = u * SUBS + sub;
+        if (r >= nvalid)
+          *reinterpret_cast<uint4*>(src + Ring<D>::box + r * D * 2 + part * 16) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    uint4 kw[U], vw[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int r = u * SUBS + sub;
-      okr[u] = in_range && tb + r < t1;
-      const uint4 kw4 = *reinterpret_cast<const uint4*>(src + r * D * 2 + part * 16);
-      const uint4 vw4 = *reinterpret_cast<const uint4*>(src + Ring<D>::box + r * D * 2 + part * 16);
-      const uint32_t kw[4] = {kw4.x, kw4.y, kw4.z, kw4.w};
-      const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 fk = unpack2<BF16>(kw[i]);
-        float2 fv = unpack2<BF16>(vw[i]);
-        kf[u][2 * i] = fk.x;
-        kf[u][2 * i + 1] = fk.y;
-        vf[u][2 * i] = okr[u] ? fv.x : 0.f;
-        vf[u][2 * i + 1] = okr[u] ? fv.y : 0.f;
-      }
+      kw[u] = *reinterpret_cast<const uint4*>(src + r * D * 2 + part * 16);
+      vw[u] = *reinterpret_cast<const uint4*>(src + Ring<D>::box + r * D * 2 + part * 16);
     }
+    const bool row_ok = r_mine < nvalid;
+    const float pos = (float)(tb + r_mine - (L - 1));   // ALiBi distance to the query
 #pragma unroll
     for (int j = 0; j < GC; ++j) {
-      float x[U];
+      float d[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float d = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d = fmaf(qr[j][i], kf[u][i], d);
-        x[u] = d;
-      }
-#pragma unroll
-      for (int off = TPG / 2; off >= 1; off >>= 1) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) x[u] += __shfl_xor_sync(0xffffffffu, x[u], off);
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        x[u] = okr[u] ? fmaf(slope[j], (float)(tb + u * SUBS + sub - (L - 1)), x[u]) : -INFINITY;
-        mx = fmaxf(mx, x[u]);
-      }
-#pragma unroll
-      for (int off = TPG; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      for (int u = 0; u < U; ++u) d[u] = dot8<BF16>(kw[u], qw[j]);
+      float x = reduce_rows<TPG, U>(d, part);
+      x = row_ok ? fmaf(x, qscale, slope[j] * pos) : -INFINITY;
+      // Maximum over the 8 rows: they differ in lane bits 2..4.
+      float mx = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       const float m_new = fmaxf(m[j], mx);
       if (m_new == -INFINITY) continue;  // nothing valid seen by this warp yet
-      const float alpha = exp2f(m[j] - m_new);
-      m[j] = m_new;
-      l[j] *= alpha;
+      if (m_new != m[j]) {               // warp-uniform: rescale only when the maximum moves
+        const float alpha = fast_exp2(m[j] - m_new);
+        l[j] *= alpha;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[j][i] *= alpha;
+        for (int i = 0; i < 8; ++i) acc[j][i] *= alpha;
+        m[j] = m_new;
+      }
+      const float pr = fast_exp2(x - m_new);   // 0 for masked rows
+      l[j] += pr;
+      const uint32_t p16 = pack2<BF16>(pr, 0.f);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float pu = exp2f(x[u] - m_new);  // 0 for masked tokens
-        l[j] += pu;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(pu, vf[u][i], acc[j][i]);
+        const uint32_t pu = __shfl_sync(0xffffffffu, p16, sub * TPG + u * kRowLanes);
+        axpy8<BF16>(acc[j], pu, vw[u]);
       }
     }
   };
@@ -291,12 +353,16 @@ __global__ void __launch_bounds__(kThreads)
     __syncwarp();
   }
 
-  // Merge the token rows (subs) of each warp: m is already warp-uniform.
+  // Merge the token rows of each warp: m is already warp-uniform; each lane's
+  // l covers the rows it held a logit for (the rows differ in lane bits 2..4,
+  // lanes differing in bits 0..1 hold copies), each lane's acc the rows of
+  // its sub-row.
 #pragma unroll
   for (int j = 0; j < GC; ++j) {
 #pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+#pragma unroll
     for (int off = TPG; off < 32; off <<= 1) {
-      l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[j][i] += __shfl_xor_sync(0xffffffffu, acc[j][i], off);
     }
