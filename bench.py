@@ -48,11 +48,11 @@ FALLBACK_HBM_GBS = 6800.0
 # the sha256 (first 16 hex digits) of the kernel source it was taken on; the
 # value is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # gather_t2048, profiles/gather_cached_kv_t2048.md: 41.97 MB read + 1.83 MB
+    # gather_t2048, profiles/gather_cached_kv_t2048.md: 41.97 MB read + 1.99 MB
     # written during the kernel (its output is still dirty in L2 when it ends)
-    "e1973fa3707e1946": 43794432,
+    "cf06688c61eaf28d": 43958272,
     # llama13b_mha_b8_ctx256, profiles/decode_simt_llama13b_mha_b8_ctx256.md
-    "a78826731fef997d": 42102272,
+    "4a694aac59655cca": 42099968,
 }
 
 
@@ -582,10 +582,10 @@ def main():
     targets = {}
     if not args.no_targets:
         for name in TARGETS:
-            us, nbytes, (ps, npx, pathx, _), ncopy = time_decode_workload(name, dev, ops)
+            us, nbytes, (ps, npx, pathx, _), tcopies = time_decode_workload(name, dev, ops)
             targets[name] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                              "path": PATH_NAMES[pathx], "partitions": npx,
-                             "copies": ncopy}
+                             "copies": tcopies}
 
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peak, peak_src = FALLBACK_HBM_GBS, "fallback"
