@@ -22,5 +22,9 @@ follows the plain definitions:
   (vLLM pull request 29).
 * ``cache`` -- writing new tokens' K/V into the pool at a slot mapping (the
   ``cache_ops.cache`` step named in the FlashAttention pull request's notes).
+* ``prefill`` -- a chunk of several new query tokens per sequence attending
+  causally over the same paged cache (the review comments of the
+  FlashAttention pull request: the KV-cache attention kernel serves prefill
+  too, with or without a cached prefix); one query per sequence is decode.
 * ``brute`` -- triple-loop dense attention on contiguous K/V, for tiny inputs.
 """

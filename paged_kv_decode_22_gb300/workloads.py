@@ -29,9 +29,9 @@ from dataclasses import dataclass, field
 import numpy as np
 
 __all__ = [
-    "f32_to_bf16_bits", "f32_to_f16_bits", "DecodeCase", "GatherCase",
-    "make_decode_case", "make_gather_case", "decode_configs", "gather_sweep",
-    "NAN_BITS",
+    "f32_to_bf16_bits", "f32_to_f16_bits", "DecodeCase", "GatherCase", "PrefillCase",
+    "make_decode_case", "make_gather_case", "make_prefill_case", "decode_configs",
+    "gather_sweep", "prefill_configs", "NAN_BITS",
 ]
 
 # Quiet-NaN bit patterns used to poison memory that no sequence references.
@@ -200,6 +200,40 @@ def make_gather_case(*, seed: int, num_tokens: int, num_heads: int, head_size: i
 
 # ---------------------------------------------------------------------------
 # The workloads.  Seed convention: 1000 * workload id + sweep index.
+
+@dataclass
+class PrefillCase:
+    """Inputs of one paged prefill call: a DecodeCase's cache, tables and
+    lengths, plus the packed chunk queries."""
+    base: DecodeCase           # its q is unused
+    q: np.ndarray              # uint16 [T, H, D], T = query_start[-1]
+    query_start: np.ndarray    # int32 [S + 1], cumulative chunk lengths
+
+    @property
+    def query_lens(self) -> np.ndarray:
+        return np.diff(self.query_start)
+
+
+def make_prefill_case(*, seed: int, num_seqs: int, num_heads: int, num_kv_heads: int,
+                      head_size: int, block_size: int, num_blocks: int, context_lens,
+                      query_lens, dtype: str, poison: bool = True,
+                      name: str = "") -> PrefillCase:
+    """A seeded paged cache (as make_decode_case) and, for each sequence s,
+    query_lens[s] new query tokens packed token-major into q [T, H, D]."""
+    base = make_decode_case(seed=seed, num_seqs=num_seqs, num_heads=num_heads,
+                            num_kv_heads=num_kv_heads, head_size=head_size,
+                            block_size=block_size, num_blocks=num_blocks,
+                            context_lens=context_lens, dtype=dtype, poison=poison,
+                            name=name or f"prefill_s{num_seqs}_h{num_heads}_{num_kv_heads}")
+    qlens = np.asarray(query_lens, dtype=np.int64).reshape(num_seqs)
+    if np.any(qlens < 0):
+        raise ValueError("query lengths must be >= 0")
+    starts = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    rng = np.random.default_rng(seed + 7919)
+    T = int(starts[-1])
+    q = _normal_bits(rng, T * num_heads * head_size, dtype).reshape(T, num_heads, head_size)
+    return PrefillCase(base=base, q=q, query_start=starts)
+
 
 def decode_configs():
     """Decode-attention workloads as {name: kwargs for make_decode_case}."""
