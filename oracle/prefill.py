@@ -24,16 +24,20 @@ slopes[h] * (t - p): the decode bias taken at the query's own position.
 
 Readings of what the page leaves open (also listed in the design notes):
   * n_s = 0 contributes no rows;
-  * a sequence with n_s > L_s, or that is invalid for decode (negative
-    length, longer than its table or than max_context_len, a bad block id
-    among t < L_s), is invalid, and all its query rows are zeros.
+  * a sequence with n_s > L_s, a negative length, or a length longer than
+    its table or than max_context_len is invalid: all its query rows are
+    zeros;
+  * a query whose window t <= p references a block id outside
+    [0, num_blocks) gives a zero row; queries before the bad block are
+    unaffected (for decode the window is the whole sequence, so this is the
+    decode rule).
 """
 from __future__ import annotations
 
 import numpy as np
 
 from .formats import decode_bits
-from .paged_attention import alibi_bias, attend, gather_sequence_kv, kv_head_of, sequence_is_valid
+from .paged_attention import alibi_bias, attend, gather_sequence_kv, kv_head_of
 
 
 def query_position(L: int, n: int, i: int) -> int:
@@ -73,15 +77,20 @@ def paged_prefill_attention(q, key_cache, value_cache, block_tables, context_len
         if n == 0:
             continue
         L = int(context_lens[s])
-        valid = sequence_is_valid(block_tables, context_lens, s, B, NB, max_context_len) and n <= L
+        length_ok = (0 <= L <= block_tables.shape[1] * B and n <= L and
+                     (max_context_len is None or L <= max_context_len))
         seq_rows = range(int(qs[s]), int(qs[s + 1]))
         if want is not None:
             seq_rows = [r for r in seq_rows if r in want]
-        if not valid:
+        if not length_ok:
             for r in seq_rows:
                 for h in range(H):
                     res[(r, h)] = np.zeros(D)
             continue
+        # First token whose block id is out of range (L if none).
+        ids = np.asarray(block_tables[s, : -(-L // B)], dtype=np.int64)
+        bad = np.nonzero((ids < 0) | (ids >= NB))[0]
+        first_bad = int(bad[0]) * B if bad.size else L
         for kv in range(Hk):
             hs = [h for h in range(H) if kv_head_of(h, H, Hk) == kv]
             K = V = None
@@ -89,11 +98,15 @@ def paged_prefill_attention(q, key_cache, value_cache, block_tables, context_len
                 heads = hs if want is None else [h for h in hs if h in want[r]]
                 if not heads:
                     continue
-                if K is None:
-                    K = gather_sequence_kv(key_cache, block_tables, s, L, kv, dtype)
-                    V = gather_sequence_kv(value_cache, block_tables, s, L, kv, dtype)
                 p = query_position(L, n, r - int(qs[s]))
                 nv = visible_tokens(p)
+                if nv > first_bad:
+                    for h in heads:
+                        res[(r, h)] = np.zeros(D)
+                    continue
+                if K is None:
+                    K = gather_sequence_kv(key_cache, block_tables, s, first_bad, kv, dtype)
+                    V = gather_sequence_kv(value_cache, block_tables, s, first_bad, kv, dtype)
                 bias = None if alibi_slopes is None else alibi_bias(alibi_slopes, heads, nv)
                 O = attend(decode_bits(q[r, heads, :], dtype), K[:nv], V[:nv], scale, bias)
                 for k, h in enumerate(heads):

@@ -144,9 +144,21 @@ def test_invalid_chunks_give_zero_rows_and_empty_chunks_give_none():
     assert out.shape == (5, 2, 8)
     assert (out[:2] == 0).all()
     assert np.isfinite(out[2:]).all() and np.abs(out[2:]).max() > 0
-    b.block_tables[2, 0] = 99               # a bad block id
+    b.block_tables[2, 0] = 99               # a bad block id under every query
     out = _run(c)
     assert (out[2:] == 0).all()
+
+
+def test_a_bad_block_zeroes_only_the_queries_that_see_it():
+    c = make_prefill_case(seed=12, num_seqs=1, num_heads=2, num_kv_heads=1, head_size=8,
+                          block_size=4, num_blocks=16, context_lens=[20], query_lens=[10],
+                          dtype="fp16")
+    b = c.base
+    good = _run(c)
+    b.block_tables[0, 3] = -7               # tokens 12..15: queries at positions >= 12
+    out = _run(c)
+    np.testing.assert_array_equal(out[:2], good[:2])      # positions 10, 11
+    assert (out[2:] == 0).all()                            # positions 12..19
 
 
 def test_sampled_rows_equal_full_output():
