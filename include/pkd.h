@@ -19,6 +19,11 @@
  *    "[Performance] Support MQA/GQA in decode phase by using
  *    FlashAttention", pull request 2744).
  *
+ *  - pkd_paged_prefill_attention: several new query tokens per sequence
+ *    (a prefill chunk, with or without a cached prefix) attending causally
+ *    over the same paged cache; the review comments of pull request 2744
+ *    note that the KV-cache attention kernel serves prefill as well.
+ *
  *  - pkd_gather_cached_kv: copies the cached K/V rows of the slots listed in
  *    a slot mapping into contiguous [num_tokens, num_heads, head_size]
  *    tensors ("Memcpy kernel for flash attention", pull request 29).
@@ -192,6 +197,43 @@ PKD_API pkd_status pkd_paged_decode_attention_static_ws(
     int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_size,
     int block_size, int num_blocks, float scale, pkd_dtype dtype, int partition_size,
     uint32_t* device_status, void* stream);
+
+/*
+ * Prefill over a paged KV cache: each sequence brings a chunk of new query
+ * tokens whose K/V rows are already in its cache as its LAST tokens (store
+ * them first with pkd_reshape_and_cache), and each query attends causally
+ * to the cache up to its own position.  With n_s = query_start[s+1] -
+ * query_start[s] and L_s = context_lens[s] (which counts the chunk), query
+ * i of sequence s (packed row r = query_start[s] + i) sits at position
+ * p = L_s - n_s + i and
+ *     out[r,h,:] = softmax_{t <= p}(scale * q[r,h,:] . K_s[t,:] + bias) @ V_s[t,:]
+ * with K_s, V_s and the query-head -> KV-head groups exactly as in
+ * pkd_paged_decode_attention; bias = alibi_slopes[h] * (t - p) when
+ * alibi_slopes is not NULL.  n_s = 1 is decode; n_s = L_s is a prompt
+ * without prefix.
+ *   out, q          [num_query_tokens][num_heads][head_size] 16-bit
+ *   query_start     [num_seqs + 1] int32, non-decreasing from 0, with
+ *                   query_start[num_seqs] == num_query_tokens (rows past
+ *                   query_start[num_seqs] are not written; a sequence whose
+ *                   rows fall outside [0, num_query_tokens) is skipped and
+ *                   sets PKD_DEV_BAD_LEN)
+ *   max_query_len   host-side upper bound of n_s (sizes the grid)
+ *   other arguments as for pkd_paged_decode_attention_ex; head_size must be
+ *   128 and num_heads / num_kv_heads at most 64 (else PKD_ERR_UNSUPPORTED).
+ * One launch of the tensor-core kernel (tcgen05 MMAs over (query, head)
+ * columns, up to 64 per work unit); no workspace.  A chunk with
+ * n_s > L_s or n_s > max_query_len, or an invalid L_s (as for decode),
+ * gives zero rows and sets PKD_DEV_BAD_LEN.  A query whose window t <= p
+ * references a block id outside [0, num_blocks) gives a zero row and sets
+ * PKD_DEV_BAD_BLOCK; the queries before that block are unaffected.
+ */
+PKD_API pkd_status pkd_paged_prefill_attention(
+    void* out, const void* q, const void* key_cache, const void* value_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    const int32_t* query_start, int num_query_tokens, int max_query_len, int max_context_len,
+    int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size, int num_blocks,
+    float scale, const float* alibi_slopes, pkd_dtype dtype, uint32_t* device_status,
+    void* stream);
 
 /*
  * gather_cached_kv: key_out[t] = key_cache[slot / block_size][slot % block_size]

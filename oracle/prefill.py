@@ -24,9 +24,9 @@ slopes[h] * (t - p): the decode bias taken at the query's own position.
 
 Readings of what the page leaves open (also listed in the design notes):
   * n_s = 0 contributes no rows;
-  * a sequence with n_s > L_s, a negative length, or a length longer than
-    its table or than max_context_len is invalid: all its query rows are
-    zeros;
+  * a sequence with n_s > L_s, a negative length, a length longer than its
+    table or than max_context_len, or a chunk longer than max_query_len is
+    invalid: all its query rows are zeros;
   * a query whose window t <= p references a block id outside
     [0, num_blocks) gives a zero row; queries before the bad block are
     unaffected (for decode the window is the whole sequence, so this is the
@@ -52,7 +52,7 @@ def visible_tokens(p: int) -> int:
 
 def paged_prefill_attention(q, key_cache, value_cache, block_tables, context_lens, query_start,
                             scale: float, dtype: str, *, max_context_len: int | None = None,
-                            alibi_slopes=None, rows=None):
+                            max_query_len: int | None = None, alibi_slopes=None, rows=None):
     """Reference prefill attention.
 
     q: uint16 bits [T, H, D] (T = query_start[-1]); key_cache / value_cache:
@@ -78,7 +78,8 @@ def paged_prefill_attention(q, key_cache, value_cache, block_tables, context_len
             continue
         L = int(context_lens[s])
         length_ok = (0 <= L <= block_tables.shape[1] * B and n <= L and
-                     (max_context_len is None or L <= max_context_len))
+                     (max_context_len is None or L <= max_context_len) and
+                     (max_query_len is None or n <= max_query_len))
         seq_rows = range(int(qs[s]), int(qs[s + 1]))
         if want is not None:
             seq_rows = [r for r in seq_rows if r in want]

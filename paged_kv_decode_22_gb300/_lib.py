@@ -32,6 +32,8 @@ _SIGS = {
                                       [_c_float, _vp, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
     "pkd_paged_decode_attention_static_ws": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
                                              [_c_float, _c_int, _c_int, _vp, _vp]),
+    "pkd_paged_prefill_attention": (_c_int, [_vp] * 5 + [_c_int, _vp, _vp] + [_c_int] * 9 +
+                                    [_c_float, _vp, _c_int, _vp, _vp]),
     "pkd_gather_cached_kv": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_vp, _vp]),
     "pkd_reshape_and_cache": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_vp, _vp]),
     "pkd_status_string": (ctypes.c_char_p, [_c_int]),
@@ -160,6 +162,37 @@ def paged_decode_attention_static_ws(out, q, key_cache, value_cache, block_table
         block_tables.shape[1], _ptr(context_lens), max_context_len, S, H, Hk, D, B, NB,
         float(scale), _dtype_code(q), partition_size, _ptr(device_status), _stream(stream))
     _check("pkd_paged_decode_attention_static_ws", st)
+    return out
+
+
+def paged_prefill_attention(out, q, key_cache, value_cache, block_tables, context_lens,
+                            query_start, max_query_len, max_context_len, scale,
+                            device_status=None, stream=None, alibi_slopes=None):
+    """Chunk queries attending causally over the paged cache.
+
+    q/out [T, H, D] (T packed query tokens); query_start int32 [S + 1];
+    key_cache/value_cache [NB, B, Hk, D]; block_tables int32 [S, MB];
+    context_lens int32 [S] (counting each chunk); alibi_slopes: None or
+    float32 [H].  Query i of sequence s sits at position
+    context_lens[s] - n_s + i and sees the cache up to that position.
+    """
+    _dense(out, q, key_cache, value_cache, block_tables, context_lens, query_start,
+           device_status, alibi_slopes)
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or
+                                     alibi_slopes.numel() != q.shape[1]):
+        raise TypeError("alibi_slopes must be float32 [num_heads]")
+    T, H, D = q.shape
+    NB, B, Hk, _ = key_cache.shape
+    S = context_lens.numel()
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or
+            query_start.dtype != torch.int32 or query_start.numel() != S + 1):
+        raise TypeError("block_tables, context_lens and query_start [S + 1] must be int32")
+    st = lib().pkd_paged_prefill_attention(
+        _ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), _ptr(query_start), T, max_query_len,
+        max_context_len, S, H, Hk, D, B, NB, float(scale), _ptr(alibi_slopes), _dtype_code(q),
+        _ptr(device_status), _stream(stream))
+    _check("pkd_paged_prefill_attention", st)
     return out
 
 

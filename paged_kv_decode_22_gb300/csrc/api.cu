@@ -217,7 +217,7 @@ pkd_status pkd_paged_decode_attention_ex(void* out, const void* q, const void* k
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKD_ERR_ALIGN;
   }
 
-  pkd::DecodeArgs a;
+  pkd::DecodeArgs a = {};
   a.out = out;
   a.q = q;
   a.key_cache = key_cache;
@@ -253,6 +253,68 @@ pkd_status pkd_paged_decode_attention_ex(void* out, const void* q, const void* k
     if (e != cudaSuccess) return cuda_fail(e, "lse_reduce launch");
   }
   return PKD_OK;
+}
+
+pkd_status pkd_paged_prefill_attention(void* out, const void* q, const void* key_cache,
+                                       const void* value_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       const int32_t* query_start, int num_query_tokens,
+                                       int max_query_len, int max_context_len, int num_seqs,
+                                       int num_heads, int num_kv_heads, int head_size,
+                                       int block_size, int num_blocks, float scale,
+                                       const float* alibi_slopes, pkd_dtype dtype,
+                                       uint32_t* device_status, void* stream) {
+  if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens || !query_start)
+    return PKD_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(alibi_slopes) & 3u) != 0) return PKD_ERR_ALIGN;
+  if (dtype != PKD_FP16 && dtype != PKD_BF16) return PKD_ERR_UNSUPPORTED;
+  if (!pow2_in(block_size, 8, 256)) return PKD_ERR_UNSUPPORTED;
+  pkd_status st = check_decode_sizes(num_seqs, num_heads, num_kv_heads, head_size, max_context_len);
+  if (st != PKD_OK) return st;
+  const int g = num_heads / num_kv_heads;
+  if (head_size != 128 || g > 64) return PKD_ERR_UNSUPPORTED;
+  if (num_query_tokens < 0 || max_query_len < 0 || num_blocks < 1 || max_blocks_per_seq < 1)
+    return PKD_ERR_SHAPE;
+  if ((long long)num_blocks * block_size > 0x7fffffffLL) return PKD_ERR_SHAPE;
+  if ((long long)max_blocks_per_seq * block_size > 0x7fff0000LL) return PKD_ERR_SHAPE;
+  if ((long long)num_query_tokens * num_heads > 0x7fffffffLL) return PKD_ERR_SHAPE;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+    return PKD_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != PKD_OK) return st;
+  if (!pkd::tma_available()) return PKD_ERR_UNSUPPORTED;
+  if (num_query_tokens == 0 || max_query_len == 0) return PKD_OK;   // no query rows
+
+  const int qt = pkd::prefill_tc_queries_per_unit(g);
+  const long long tiles = ((long long)max_query_len + qt - 1) / qt;
+  if (tiles > 65535) return PKD_ERR_SHAPE;
+  pkd::DecodeArgs a = {};
+  a.out = out;
+  a.q = q;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.alibi = alibi_slopes;
+  a.is_bf16 = dtype == PKD_BF16;
+  a.partition_size = max_context_len;   // unused by prefill: one range per query tile
+  a.num_partitions = (int)tiles;        // query tiles per sequence, at most
+  a.query_start = query_start;
+  a.q_per_unit = qt;
+  a.max_query_len = max_query_len;
+  a.num_q_tokens = num_query_tokens;
+  a.status = device_status;
+  cudaError_t e = pkd::launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKD_OK : cuda_fail(e, "prefill launch");
 }
 
 static pkd_status copy_common(const void* a, const void* b, const void* c, const void* d,

@@ -85,13 +85,14 @@ struct Misc {
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], drain;
   uint32_t tmem_base;
   int abort;
-  int k_bad[3];                 // per K stage: the tile referenced a bad block id
+  int k_bad[3];                 // per K stage: token offset of the tile's first bad block id, or -1
   alignas(16) float red[2][4][64];   // per-warp tile maxima
   alignas(16) float m_run[64];       // running maxima (log2 domain)
   alignas(16) float alpha[2][64];    // rescale factor of each tile parity
   float lsum[4][64];            // per-warp exponent sums at finalisation
   alignas(16) float inv_l[64];       // 1 / sum (0 for a bad unit)
-  alignas(16) float slope[64];       // ALiBi slopes of the unit's heads (log2 units)
+  alignas(16) float slope[64];       // ALiBi slopes of the unit's columns (log2 units)
+  alignas(16) int lim[64];           // prefill: last visible position of each column (-1: none)
   float sum_l[64];                   // sum written to the workspace
   SchedSmem sched;                   // work-unit schedule
 };
@@ -194,7 +195,7 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[CH]) {
 }
 
 
-template <bool BF16, int NPAD>
+template <bool BF16, int NPAD, bool PF>
 __global__ void __launch_bounds__(threads_of(NPAD), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     for (int i = 0; i < NK; ++i) {
       mbar_init(&ms.k_full[i], 1);
       mbar_init(&ms.k_empty[i], 1 + kSoftmaxThreads * GROUPS);
-      ms.k_bad[i] = 0;
+      ms.k_bad[i] = -1;
     }
     for (int i = 0; i < NV; ++i) {
       mbar_init(&ms.v_full[i], 1);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     };
     UnitCursor cur = cursor_begin(ms.sched, a);
     UnitInfo ui;
-    bool have = cursor_next<TT>(cur, ms.sched, a, ui);
+    bool have = cursor_next<TT, PF>(cur, ms.sched, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       bool nhave = true;
       int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nhave = cursor_next<TT>(cur, ms.sched, a, nui);
+        nhave = cursor_next<TT, PF>(cur, ms.sched, a, nui);
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
@@ -306,23 +307,32 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         const int qb = un & 1;
         ok = mbar_wait(&ms.q_empty[qb], ((un >> 1) & 1) ^ 1);
         if (ok) {
-          mbar_arrive_expect_tx(&ms.q_full[qb], LY::QB);
-          const int row0 = ui.s * a.num_heads + ui.hk * g;
-          tma_load_2d(qbuf + qb * LY::QB, &qmap, &ms.q_full[qb], 0, row0);
-          tma_load_2d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, row0);
+          if constexpr (PF) {
+            // Chunk queries [qrow0, qrow0 + QT) x the group's g heads: rows
+            // (query, head) of the q operand, box {64, g, QT}.
+            mbar_arrive_expect_tx(&ms.q_full[qb], (uint32_t)(g * a.q_per_unit * 256));
+            tma_load_3d(qbuf + qb * LY::QB, &qmap, &ms.q_full[qb], 0, ui.hk * g, ui.qrow0);
+            tma_load_3d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, ui.hk * g,
+                        ui.qrow0);
+          } else {
+            mbar_arrive_expect_tx(&ms.q_full[qb], LY::QB);
+            const int row0 = ui.s * a.num_heads + ui.hk * g;
+            tma_load_2d(qbuf + qb * LY::QB, &qmap, &ms.q_full[qb], 0, row0);
+            tma_load_2d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, row0);
+          }
         }
       }
       const int ts = ui.t0 + jl * TT;
       const bool bad = raw != kNoBlock && (raw < 0 || raw >= a.num_blocks);
       const int row = (raw != kNoBlock && !bad) ? raw * B + (B <= TT ? 0 : ts % B) : oob_row;
-      const bool any_bad = __any_sync(0xffffffffu, bad);
+      const uint32_t bad_lanes = __ballot_sync(0xffffffffu, bad);   // lanes < nbox: boxes in token order
       const int st = jk % nst;
       if (lane == 0) {
         ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
         if (ok) {
           if (!is_v) {
-            ms.k_bad[st] = any_bad ? 1 : 0;
-            if (any_bad) flag(a.status, PKD_DEV_BAD_BLOCK);
+            ms.k_bad[st] = bad_lanes ? (__ffs(bad_lanes) - 1) * R : -1;
+            if (bad_lanes) flag(a.status, PKD_DEV_BAD_BLOCK);
           }
           mbar_arrive_expect_tx(&full[st], TILE_BYTES);
         }
@@ -376,7 +386,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       };
       UnitCursor cur = cursor_begin(ms.sched, a);
       UnitInfo ui;
-      while (ok && cursor_next<TT>(cur, ms.sched, a, ui)) {
+      while (ok && cursor_next<TT, PF>(cur, ms.sched, a, ui)) {
         // The softmax warps finish the previous unit only after its last P V:
         // issue that one before this unit's first S.
         if (prev >= 0) {
@@ -435,7 +445,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     const bool single = a.num_partitions == 1;
     const bool fused = a.fused != 0;           // one unit, merged over the cluster
     const int H = a.num_heads;
-    const int my_heads = max(0, min(HPG, g - hbase));    // valid heads of this warpgroup
+    const int group_heads = max(0, min(HPG, g - hbase));    // decode: valid heads of this warpgroup
     float o_acc[HPG], l_part[HPG];
 #pragma unroll
     for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
@@ -464,10 +474,23 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     UnitCursor cur = cursor_begin(ms.sched, a);
     UnitInfo ui;
     const bool alibi = a.alibi != nullptr;
-    while (ok && cursor_next<TT>(cur, ms.sched, a, ui)) {
+    while (ok && cursor_next<TT, PF>(cur, ms.sched, a, ui)) {
       const int h0 = ui.hk * g;
+      // Valid columns of this warpgroup: decode, the group's heads; prefill,
+      // the unit's (query, head) pairs c = query * g + head.
+      const int my_heads = PF ? max(0, min(HPG, ui.nq * g - hbase)) : group_heads;
       bool unit_bad = false;
-      if (alibi) {
+      int bad_from = 0x7fffffff;       // prefill: first token of a bad block seen so far
+      if constexpr (PF) {
+        // Last visible position and slope of each column.
+        const int ncols = ui.nq * g;
+        if (et < HPG) {
+          const int c = hbase + et;
+          ms.lim[c] = c < ncols ? ui.pos0 + c / g : -1;
+          if (alibi) ms.slope[c] = c < ncols ? a.alibi[h0 + c % g] * kLog2e : 0.f;
+        }
+        named_barrier(bar, kSoftmaxThreads);
+      } else if (alibi) {
         if (et < my_heads) ms.slope[hbase + et] = a.alibi[h0 + hbase + et] * kLog2e;
         named_barrier(bar, kSoftmaxThreads);
       }
@@ -480,7 +503,12 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         ok = ok && mbar_wait(&ms.s_full[b], (j >> 1) & 1);
         ok = ok && mbar_wait(&ms.k_full[ks], (j / NK) & 1);
         tc_fence_after();
-        unit_bad |= ms.k_bad[ks] != 0;
+        if constexpr (PF) {
+          const int kb = ms.k_bad[ks];
+          if (kb >= 0) bad_from = min(bad_from, ts + kb);
+        } else {
+          unit_bad |= ms.k_bad[ks] >= 0;
+        }
         mbar_arrive(&ms.k_empty[ks]);
         // Tile maxima per head (logits kept in registers for the exponentials).
         const uint32_t s_addr = lane_addr + b * NPAD + hbase;
@@ -490,7 +518,25 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         for (int c = 0; c < NCH; ++c) {
           float x[CH];
           tmem_ld<CH>(s_addr + c * CH, x);
-          if (alibi) {
+          if constexpr (PF) {
+            // Causal mask per column: token ts + row is visible to column i
+            // when it does not pass that query's position.
+            int lm[CH];
+            float sl[CH];
+#pragma unroll
+            for (int i = 0; i < CH; i += 4) {
+              *reinterpret_cast<int4*>(&lm[i]) =
+                  *reinterpret_cast<const int4*>(&ms.lim[hbase + c * CH + i]);
+              *reinterpret_cast<float4*>(&sl[i]) =
+                  *reinterpret_cast<const float4*>(&ms.slope[hbase + c * CH + i]);
+            }
+            const int t = ts + row;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+              const float b = alibi ? sl[i] * (float)(t - lm[i]) : 0.f;
+              x[i] = t <= lm[i] ? fmaf(x[i], qscale, b) : -INFINITY;
+            }
+          } else if (alibi) {
             float sl[CH];
 #pragma unroll
             for (int i = 0; i < CH; i += 4)
@@ -582,10 +628,33 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       if (et < my_heads) {
         const int h = hbase + et;
         const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
-        ms.inv_l[h] = unit_bad || den == 0.f ? 0.f : 1.f / den;
-        ms.sum_l[h] = unit_bad ? -1.f : den;
+        // Prefill: a column is bad when its window reaches a bad block.
+        const bool bad = PF ? ms.lim[h] >= bad_from : unit_bad;
+        ms.inv_l[h] = bad || den == 0.f ? 0.f : 1.f / den;
+        ms.sum_l[h] = bad ? -1.f : den;
       }
       named_barrier(bar, kSoftmaxThreads);
+      if constexpr (PF) {
+        // Column c = (query c / g, head c % g) -> out row qrow0 + c / g, head
+        // h0 + c % g; this thread writes element d = row of each column.
+#pragma unroll
+        for (int hl = 0; hl < HPG; ++hl) {
+          if (hl < my_heads) {
+            const int c = hbase + hl;
+            const int qi = c / g;
+            const size_t orow = (size_t)(ui.qrow0 + qi) * H + h0 + (c - qi * g);
+            static_cast<uint16_t*>(a.out)[orow * HD + row] =
+                (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[c], 0.f);
+          }
+        }
+        if (et < my_heads) ms.m_run[hbase + et] = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
+        // The next unit's column set may differ: every thread is done with
+        // this unit's lim / inv_l before they are rewritten.
+        named_barrier(bar, kSoftmaxThreads);
+        continue;
+      }
       // Stage this warpgroup's output rows in its own P rows (idle now: the
       // unit's last P V has completed) and write them with bulk copies.  The
       // warpgroup's P rows are four pieces of HPG x 128 bytes (2 buffers x 2
@@ -712,7 +781,7 @@ int pad_group(int g) { return (g + 15) / 16 * 16; }
 
 // Kernel attributes, set once per device: the dynamic shared memory and
 // clusters of up to 16 CTAs.
-template <bool BF16, int NPAD>
+template <bool BF16, int NPAD, bool PF = false>
 cudaError_t prepare(int* smem_out) {
   const int smem = SmemLayout<NPAD>::bytes + 1024;
   *smem_out = smem;
@@ -721,9 +790,9 @@ cudaError_t prepare(int* smem_out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || attr_set[dev]) return cudaSuccess;
-  if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
+  if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD, PF>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
+      (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD, PF>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
     return e;
   attr_set[dev] = true;
@@ -765,15 +834,38 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
     cudaLaunchAttribute attr[2];
     cluster_config(&cfg, attr, dim3(a.num_partitions, a.num_seqs * a.num_kv_heads),
                    threads_of(NPAD), smem, a.num_partitions, st);
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BF16, NPAD>, km, vm, qm, a);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BF16, NPAD, false>, km, vm, qm, a);
   }
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   const int grid = (int)(units < sms ? units : sms);
-  return launch_pdl(decode_tc_kernel<BF16, NPAD>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
+  return launch_pdl(decode_tc_kernel<BF16, NPAD, false>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
                     km, vm, qm, a);
+}
+
+// Prefill: persistent grid over (sequence, KV head, query tile) units.
+template <bool BF16, int NPAD>
+cudaError_t launch_pf(const DecodeArgs& a, cudaStream_t st) {
+  CUtensorMap km, vm, qm;
+  const long long rows = (long long)a.num_blocks * a.block_size;
+  const int box_rows = a.block_size < TT ? a.block_size : TT;
+  const int g = a.num_heads / a.num_kv_heads;
+  if (!make_kv_map(&km, a.key_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
+      !make_kv_map(&vm, a.value_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
+      !make_q_chunk_map(&qm, a.q, BF16, HD, a.num_heads, a.num_q_tokens, g, a.q_per_unit))
+    return cudaErrorInvalidValue;
+  int smem = 0;
+  cudaError_t e = prepare<BF16, NPAD, true>(&smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  const int grid = (int)(units < sms ? units : sms);
+  return launch_pdl(decode_tc_kernel<BF16, NPAD, true>, dim3(grid), dim3(threads_of(NPAD)), smem,
+                    st, km, vm, qm, a);
 }
 
 // Co-resident clusters of `cluster` CTAs, cached per device and cluster size.
@@ -789,7 +881,8 @@ int capacity_t(int cluster) {
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr[2];
       cluster_config(&cfg, attr, dim3(cluster), threads_of(NPAD), smem, cluster, nullptr);
-      if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<true, NPAD>, &cfg) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<true, NPAD, false>, &cfg) !=
+          cudaSuccess) {
         cudaGetLastError();   // a refused query only means "no cluster launch"
         n = 0;
       }
@@ -817,6 +910,17 @@ bool decode_tc_supported(int head_size, int group, int block_size) {
 }
 
 int decode_tc_tile() { return TT; }
+
+int prefill_tc_queries_per_unit(int group) { return group >= 1 && group <= 64 ? 64 / group : 0; }
+
+cudaError_t launch_prefill_tc(const DecodeArgs& a, cudaStream_t st) {
+  const int g = a.num_heads / a.num_kv_heads;
+  if (a.head_size != HD || a.q_per_unit != prefill_tc_queries_per_unit(g)) return cudaErrorInvalidValue;
+  const int cols = pad_group(g * a.q_per_unit);
+  if (cols == 48) return a.is_bf16 ? launch_pf<true, 48>(a, st) : launch_pf<false, 48>(a, st);
+  if (cols == 64) return a.is_bf16 ? launch_pf<true, 64>(a, st) : launch_pf<false, 64>(a, st);
+  return cudaErrorNotSupported;
+}
 
 int decode_tc_cluster_capacity(int group, int cluster) {
   if (cluster < 2 || cluster > kMaxCluster || group < 4 || group > 64) return 0;

@@ -50,6 +50,10 @@ struct DecodeArgs {
   int fused;            // tensor-core path only: the partitions of one (sequence,
                         // KV head) form one thread-block cluster and are merged
                         // through distributed shared memory (no workspace)
+  const int32_t* query_start;   // prefill: [S + 1] cumulative chunk lengths (nullptr: decode)
+  int q_per_unit;       // prefill: query tokens per work unit
+  int max_query_len;    // prefill: longer chunks are invalid (zero rows)
+  int num_q_tokens;     // prefill: rows of q and out (query_start[S])
   float* ws_o;          // [S][Hk][P][H/Hk][D] unnormalised partial outputs
   float* ws_m;          // [S][Hk][P][H/Hk] partial maxima (log2 domain)
   float* ws_l;          // [S][Hk][P][H/Hk] partial sums; < 0 marks a bad block
@@ -77,6 +81,10 @@ bool make_kv_map(CUtensorMap* map, const void* cache, bool bf16, int head_size, 
                  long long rows, int box_cols, int box_rows, bool swizzle128);
 bool make_rows_map(CUtensorMap* map, const void* base, bool bf16, int cols, long long rows,
                    int box_cols, int box_rows);
+// Query chunks: 3-D {head_size, num_heads, tokens} over q [tokens][H][D],
+// box {64, box_heads, box_tokens}, 128-byte swizzle.
+bool make_q_chunk_map(CUtensorMap* map, const void* q, bool bf16, int head_size, int num_heads,
+                      long long tokens, int box_heads, int box_tokens);
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t st);
 int simt_heads_per_cta(int group);
@@ -86,6 +94,10 @@ int decode_tc_tile();
 // Clusters of `cluster` CTAs of the tensor-core kernel for query-group size
 // `group` that the current device holds at once (0: cannot launch).
 int decode_tc_cluster_capacity(int group, int cluster);
+// Prefill on the tensor-core kernel: query tokens per work unit for a
+// query-group size (their columns fill at most 64 MMA columns), and the launch.
+int prefill_tc_queries_per_unit(int group);
+cudaError_t launch_prefill_tc(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st);

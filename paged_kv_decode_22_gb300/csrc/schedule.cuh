@@ -10,6 +10,8 @@
 // With more sequences CTAs take units round-robin and skip the empty ones.
 // In the cluster form of the tensor-core kernel each CTA takes the single
 // unit its grid position names (x = partition, y = sequence * Hk + KV head).
+// For prefill a unit is (sequence, KV head, query tile) and reads the cache
+// from token 0 up to the position of the tile's last query.
 #pragma once
 
 #include "common.cuh"
@@ -28,6 +30,10 @@ struct SchedSmem {
 struct UnitInfo {
   int s, hk, p, L, t0, t1, ntiles;
   bool lok;
+  // Prefill only: the unit's queries are chunk queries [p * QT, p * QT + nq)
+  // of sequence s, stored from packed row qrow0 on; the first sits at
+  // position pos0, query c at pos0 + c.
+  int qrow0, nq, pos0;
 };
 
 __device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
@@ -36,7 +42,38 @@ __device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
              : 0;
 }
 
+// Prefill: a sequence's units are its query tiles of q_per_unit queries; a
+// chunk longer than the context or than max_query_len (or an invalid
+// length) has none.
+__device__ __forceinline__ bool chunk_rows_ok(const DecodeArgs& a, int s) {
+  const int q0 = a.query_start[s], q1 = a.query_start[s + 1];
+  return 0 <= q0 && q0 <= q1 && q1 <= a.num_q_tokens;   // rows inside q / out
+}
+
+__device__ __forceinline__ int prefill_parts(const DecodeArgs& a, int s, int L) {
+  const int n = a.query_start[s + 1] - a.query_start[s];
+  return (chunk_rows_ok(a, s) && len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) &&
+          n > 0 && n <= L && n <= a.max_query_len)
+             ? (n + a.q_per_unit - 1) / a.q_per_unit
+             : 0;
+}
+
+// Token range and queries of prefill unit (s, query tile p): the unit reads
+// the cache up to its last query's position.
 template <int TT>
+__device__ __forceinline__ void prefill_unit(const DecodeArgs& a, UnitInfo& ui) {
+  const int q0 = a.query_start[ui.s];
+  const int n = a.query_start[ui.s + 1] - q0;
+  const int i0 = ui.p * a.q_per_unit;
+  ui.nq = min(a.q_per_unit, n - i0);
+  ui.qrow0 = q0 + i0;
+  ui.pos0 = ui.L - n + i0;
+  ui.t0 = 0;
+  ui.t1 = ui.pos0 + ui.nq;
+  ui.ntiles = (ui.t1 + TT - 1) / TT;
+}
+
+template <int TT, bool PF>
 __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
   UnitInfo ui;
   const int P = a.num_partitions;
@@ -46,6 +83,10 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
   ui.s = sh / a.num_kv_heads;
   ui.L = a.context_lens[ui.s];
   ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
+  if constexpr (PF) {
+    if (ui.p < prefill_parts(a, ui.s, ui.L)) prefill_unit<TT>(a, ui); else ui.ntiles = 0;
+    return ui;
+  }
   ui.t0 = ui.p * a.partition_size;
   ui.t1 = min(ui.t0 + a.partition_size, ui.L);
   ui.ntiles = (ui.lok && ui.t0 < ui.L) ? (ui.t1 - ui.t0 + TT - 1) / TT : 0;
@@ -75,7 +116,8 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
   return c;
 }
 
-template <int TT>
+// PF: prefill units (a.query_start set), else decode units.
+template <int TT, bool PF = false>
 __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
                                             const DecodeArgs& a, UnitInfo& ui) {
   if (c.dense) {
@@ -88,18 +130,22 @@ __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
     }
     ui.s = lo;
     ui.L = sc.L[lo];
-    const int np = parts_of(a, ui.L);
+    const int np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;   // units per KV head
     const int r = j - sc.pre[lo];
     ui.hk = r / np;
     ui.p = r - ui.hk * np;
     ui.lok = true;
+    if constexpr (PF) {
+      prefill_unit<TT>(a, ui);
+      return true;
+    }
     ui.t0 = ui.p * a.partition_size;
     ui.t1 = min(ui.t0 + a.partition_size, ui.L);
     ui.ntiles = (ui.t1 - ui.t0 + TT - 1) / TT;
     return true;
   }
   while (c.next < c.end) {
-    ui = unit_info<TT>(a, (int)c.next);
+    ui = unit_info<TT, PF>(a, (int)c.next);
     c.next += gridDim.x;
     if (ui.ntiles) return true;
   }
@@ -120,7 +166,7 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
     for (int i = threadIdx.x; i < a.num_seqs; i += nthreads) {
       const int L = a.context_lens[i];
       sc.L[i] = L;
-      sc.pre[i + 1] = parts_of(a, L) * a.num_kv_heads;
+      sc.pre[i + 1] = (a.query_start ? prefill_parts(a, i, L) : parts_of(a, L)) * a.num_kv_heads;
     }
     __syncthreads();
     if (warp == 0) {
@@ -140,6 +186,24 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
         sc.total = carry;
       }
     }
+  }
+  if (a.query_start) {
+    // Prefill: zero the query rows of chunks that cannot be attended (an
+    // invalid length, or longer than the context) and flag them.
+    for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
+      const int L = a.context_lens[sq];
+      const int q0 = a.query_start[sq], n = a.query_start[sq + 1] - q0;
+      if (!chunk_rows_ok(a, sq)) {         // rows outside q / out: nothing can be written
+        if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
+      } else if (n > 0 && prefill_parts(a, sq, L) == 0) {
+        if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
+        uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)q0 * a.num_heads * a.head_size / 2;
+        const size_t words = (size_t)n * a.num_heads * a.head_size / 2;
+        for (size_t i = threadIdx.x; i < words; i += nthreads) o[i] = 0u;
+      }
+    }
+    __syncthreads();
+    return;
   }
   for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
     const int L = a.context_lens[sq];

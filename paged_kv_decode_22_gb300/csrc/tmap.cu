@@ -59,4 +59,18 @@ bool make_rows_map(CUtensorMap* map, const void* base, bool bf16, int cols, long
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_q_chunk_map(CUtensorMap* map, const void* q, bool bf16, int head_size, int num_heads,
+                      long long tokens, int box_heads, int box_tokens) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_size, (cuuint64_t)num_heads, (cuuint64_t)tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_size * 2, (cuuint64_t)num_heads * head_size * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pkd
