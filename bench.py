@@ -43,6 +43,7 @@ TARGETS = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "gqa_ctx409
 PATH_NAMES = {0: "simt", 1: "tc", 2: "tc_cluster"}   # decode_plan's kernel family
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by
 # the sha256 (first 16 hex digits) of the kernel source it was taken on; the
@@ -316,6 +317,71 @@ def device_decode_inputs(name, dev):
                 scale=1.0 / math.sqrt(D), out=torch.empty_like(q), bytes=nbytes)
 
 
+def prefill_work(lens, qlens, H, Hk, D):
+    """(causal FLOPs, algorithmic bytes) of one prefill call: each query at
+    position p costs 4*D FLOPs per visible token and head (q.K and p.V);
+    bytes are every sequence's K/V read once plus q read and out written."""
+    flops = 0
+    for L, n in zip(lens, qlens):
+        vis = n * (L - n) + n * (n + 1) // 2          # sum over queries of (p + 1)
+        flops += 4 * D * H * vis
+    kv = sum(lens) * Hk * D * 2 * 2
+    qo = 2 * sum(qlens) * H * D * 2
+    return flops, kv + qo
+
+
+def device_prefill_inputs(name, dev):
+    """Device inputs of a prefill workload from a seeded torch generator."""
+    import torch
+
+    from paged_kv_decode_22_gb300.workloads import prefill_configs
+    cfg = prefill_configs()[name]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg["seed"])
+    S, H, Hk, D, B = (cfg["num_seqs"], cfg["num_heads"], cfg["num_kv_heads"], cfg["head_size"],
+                      cfg["block_size"])
+    lens = torch.tensor(cfg["context_lens"], dtype=torch.int32)
+    qlens = torch.tensor(cfg["query_lens"], dtype=torch.int32)
+    need = (lens + B - 1) // B
+    nb = max(cfg["num_blocks"], int(need.sum()))
+    dt = torch.float16 if cfg["dtype"] == "fp16" else torch.bfloat16
+    T = int(qlens.sum())
+    kc = torch.randn((nb, B, Hk, D), generator=gen, device=dev, dtype=dt)
+    vc = torch.randn((nb, B, Hk, D), generator=gen, device=dev, dtype=dt)
+    q = torch.randn((T, H, D), generator=gen, device=dev, dtype=dt)
+    perm = torch.randperm(nb, generator=gen, device=dev).to(torch.int32)
+    bt = torch.zeros((S, int(need.max())), dtype=torch.int32, device=dev)
+    pos = 0
+    for si in range(S):
+        n = int(need[si])
+        bt[si, :n] = perm[pos:pos + n]
+        pos += n
+    qs = torch.zeros(S + 1, dtype=torch.int32)
+    qs[1:] = torch.cumsum(qlens, 0)
+    flops, nbytes = prefill_work(lens.tolist(), qlens.tolist(), H, Hk, D)
+    return dict(q=q, kc=kc, vc=vc, bt=bt, cl=lens.to(dev), qs=qs.to(dev), max_q=int(qlens.max()),
+                max_ctx=int(lens.max()), scale=1.0 / math.sqrt(D), out=torch.empty_like(q),
+                flops=flops, bytes=nbytes)
+
+
+def time_prefill_workload(name, dev, ops):
+    """(us per call, FLOPs, bytes, copies) of one prefill workload, inputs
+    rotated over enough copies to exceed 3x L2."""
+    import torch
+    d0 = device_prefill_inputs(name, dev)
+    ncopy = max(1, min(8, math.ceil(3 * L2_BYTES / d0["bytes"])))
+    sets = [d0] + [dict(d0, q=d0["q"].clone(), kc=d0["kc"].clone(), vc=d0["vc"].clone(),
+                        out=torch.empty_like(d0["out"])) for _ in range(ncopy - 1)]
+    fns = [lambda d=d: ops.paged_prefill_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"],
+                                                   d["cl"], d["qs"], d["max_q"], d["max_ctx"],
+                                                   d["scale"]) for d in sets]
+    us = graph_time(fns)
+    out = (us, d0["flops"], d0["bytes"], ncopy)
+    del d0, sets, fns
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_profile(args, local):
     """Run one kernel family on one workload (no timing): the command ncu wraps."""
     import torch
@@ -335,6 +401,12 @@ def run_profile(args, local):
         def call():
             ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"], d["cl"],
                                        d["max_ctx"], d["scale"], workspace=work)
+    elif kind == "prefill":
+        d = device_prefill_inputs(name, dev)
+
+        def call():
+            ops.paged_prefill_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"], d["cl"],
+                                        d["qs"], d["max_q"], d["max_ctx"], d["scale"])
     elif kind == "gather":
         g = make_gather_case(name=name, **gather_sweep()[name])
         import numpy as np
@@ -365,7 +437,7 @@ def run_sweep(args, local):
 
     from paged_kv_decode_22_gb300 import ops
     from paged_kv_decode_22_gb300.workloads import (decode_configs, gather_sweep,
-                                                    make_gather_case)
+                                                    make_gather_case, prefill_configs)
     import numpy as np
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -381,6 +453,19 @@ def run_sweep(args, local):
                           "frac": round(nbytes / us / 1e3 / peak, 3),
                           "path": PATH_NAMES[path], "partitions": npart,
                           "partition_size": ps, "bytes": nbytes, "copies": ncopy}), flush=True)
+    tpeak = None
+    if os.path.exists(pk_path):
+        with open(pk_path) as f:
+            tpeak = json.load(f).get("bf16_tflops")
+    tpeak = float(tpeak or FALLBACK_BF16_TFLOPS)
+    for name in prefill_configs():
+        us, flops, nbytes, ncopy = time_prefill_workload(name, dev, ops)
+        tf = flops / us / 1e6
+        print(json.dumps({"workload": name, "kind": "prefill", "us_per_call": round(us, 2),
+                          "TFLOPs": round(tf, 1), "frac_tensor": round(tf / tpeak, 3),
+                          "GBps": round(nbytes / us / 1e3, 1),
+                          "frac_hbm": round(nbytes / us / 1e3 / peak, 3), "flops": flops,
+                          "bytes": nbytes, "copies": ncopy}), flush=True)
     for name, cfg in gather_sweep().items():
         g = make_gather_case(name=name, **cfg)
         up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
@@ -415,7 +500,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time every decode workload and gather point (one JSON line each)")
     ap.add_argument("--profile", default=None, metavar="KIND:NAME",
-                    help="profiling mode: run only 'decode:<workload>' or 'gather:<workload>' "
+                    help="profiling mode: run only 'decode:<workload>', 'prefill:<workload>' or "
+                         "'gather:<workload>' "
                          "warmup + steps times (no timing, no JSON line), e.g. under ncu")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

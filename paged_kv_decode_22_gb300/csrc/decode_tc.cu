@@ -56,11 +56,14 @@ constexpr int kNoBlock = -2147483647 - 1;  // "no block here" marker of the prod
 constexpr uint32_t kSoftmaxBar = 1;     // named barrier id of softmax group 0 (group 1: 2)
 constexpr int kMaxCluster = 16;         // partitions merged inside one cluster, at most
 
-__host__ __device__ constexpr int k_stages(int npad) { return npad <= 48 ? 3 : 2; }
-__host__ __device__ constexpr int v_stages(int npad) { return npad <= 16 ? 3 : 2; }
-// Query heads of a group are split between 1 or 2 softmax warpgroups; each
-// handles HPG heads in chunks of CH columns.
-__host__ __device__ constexpr int sm_groups(int npad) { return npad >= 32 ? 2 : 1; }
+// K stages recycle as soon as S = K q^T has run; V stages only after P V,
+// which waits for the softmax, so V gets the deeper ring where shared memory
+// allows only five stages.
+__host__ __device__ constexpr int k_stages(int npad) { return npad <= 16 ? 3 : 2; }
+__host__ __device__ constexpr int v_stages(int npad) { return npad <= 48 ? 3 : 2; }
+// The NPAD columns of S and O (the query group padded to a multiple of 16)
+// are split between NPAD / 16 softmax warpgroups of 16 columns each.
+__host__ __device__ constexpr int sm_groups(int npad) { return npad / 16; }
 __host__ __device__ constexpr int threads_of(int npad) { return 64 + 128 * sm_groups(npad) + 32; }
 __host__ __device__ constexpr int tmem_cols(int npad) {
   return 4 * npad <= 32 ? 32 : 4 * npad <= 64 ? 64 : 4 * npad <= 128 ? 128 : 256;
@@ -76,7 +79,7 @@ struct SmemLayout {
   static constexpr int off_q = off_v + NV * TILE_BYTES;
   static constexpr int off_p = off_q + 2 * QB;
   static constexpr int off_misc = off_p + 2 * QB;
-  static constexpr int misc_bytes = 13312;
+  static constexpr int misc_bytes = 14848;
   static constexpr int bytes = off_misc + misc_bytes;
 };
 
@@ -87,12 +90,13 @@ struct Misc {
   int abort;
   int k_bad[3];                 // per K stage: token offset of the tile's first bad block id, or -1
   alignas(16) float red[2][4][64];   // per-warp tile maxima
-  alignas(16) float m_run[64];       // running maxima (log2 domain)
+  alignas(16) float m_run[2][64];    // reference maxima (log2 domain), per unit parity
   alignas(16) float alpha[2][64];    // rescale factor of each tile parity
   float lsum[4][64];            // per-warp exponent sums at finalisation
   alignas(16) float inv_l[64];       // 1 / sum (0 for a bad unit)
-  alignas(16) float slope[64];       // ALiBi slopes of the unit's columns (log2 units)
-  alignas(16) int lim[64];           // prefill: last visible position of each column (-1: none)
+  alignas(16) float slope[2][64];    // ALiBi slopes of the unit's columns (log2 units)
+  alignas(16) int lim[2][64];        // prefill: last visible position of each column (-1: none)
+  int orow[2][64];                   // prefill: output row (token * H + head) of each column
   float sum_l[64];                   // sum written to the workspace
   SchedSmem sched;                   // work-unit schedule
 };
@@ -102,12 +106,6 @@ static_assert(sizeof(Misc) <= SmemLayout<16>::misc_bytes, "misc area too small")
 __device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
   ms.abort = 1;
   flag(status, PKD_DEV_TIMEOUT);
-}
-
-// Position of element (row r, 16-bit column c) inside a K-major operand made
-// of 128-byte swizzled slabs of 64 columns, `rows` rows per slab.
-__device__ __forceinline__ int sw128_offset(int r, int c, int rows) {
-  return (c >> 6) * rows * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1);
 }
 
 // Maximum over the 32 lanes of each of 16 per-lane values, by a butterfly
@@ -129,35 +127,6 @@ __device__ __forceinline__ float warp_max16(const float (&v)[16], int lane) {
   return fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
 }
 
-// 8-value versions: lane l ends with the result for value (l >> 2) & 7.
-__device__ __forceinline__ float warp_max8(const float (&v)[8], int lane) {
-  float w4[4], w2[2];
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    w4[i] = fmaxf(b4 ? v[4 + i] : v[i], __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16));
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-    w2[i] = fmaxf(b3 ? w4[2 + i] : w4[i], __shfl_xor_sync(0xffffffffu, b3 ? w4[i] : w4[2 + i], 8));
-  float w1 = fmaxf(b2 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4));
-  w1 = fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 2));
-  return fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
-}
-
-__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
-  float w4[4], w2[2];
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    w4[i] = (b4 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16);
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-    w2[i] = (b3 ? w4[2 + i] : w4[i]) + __shfl_xor_sync(0xffffffffu, b3 ? w4[i] : w4[2 + i], 8);
-  float w1 = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
-  w1 += __shfl_xor_sync(0xffffffffu, w1, 2);
-  return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
-}
-
 // Same butterfly for sums: lane l ends with the sum of value (l >> 1) & 15.
 __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
   float w8[8], w4[4], w2[2];
@@ -174,26 +143,6 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
   float w1 = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
   return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
 }
-
-template <int CH>
-__device__ __forceinline__ float chunk_max(const float (&v)[CH], int lane) {
-  if constexpr (CH == 16) return warp_max16(v, lane); else return warp_max8(v, lane);
-}
-template <int CH>
-__device__ __forceinline__ float chunk_sum(const float (&v)[CH], int lane) {
-  if constexpr (CH == 16) return warp_sum16(v, lane); else return warp_sum8(v, lane);
-}
-// Lane that holds a chunk reduction's result for value i, and the value a lane holds.
-template <int CH>
-__device__ __forceinline__ bool chunk_writer(int lane) { return (lane & (32 / CH - 1)) == 0; }
-template <int CH>
-__device__ __forceinline__ int chunk_index(int lane) { return (lane / (32 / CH)) & (CH - 1); }
-
-template <int CH>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[CH]) {
-  if constexpr (CH == 16) tmem_ld16(taddr, v); else tmem_ld8(taddr, v);
-}
-
 
 template <bool BF16, int NPAD, bool PF>
 __global__ void __launch_bounds__(threads_of(NPAD), 1)
@@ -245,7 +194,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   // P buffers start at zero: rows of padded heads are never written again.
   for (int i = threadIdx.x; i < 2 * LY::QB / 16; i += kThreads)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = threadIdx.x; i < 64; i += kThreads) ms.m_run[i] = -INFINITY;
+  for (int i = threadIdx.x; i < 128; i += kThreads) ms.m_run[i >> 6][i & 63] = -INFINITY;
   if (warp == 1) {
     tmem_alloc(&ms.tmem_base, tmem_cols(NPAD));
     tmem_relinquish();
@@ -426,13 +375,22 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     __syncwarp();
   } else {
     // ============================================================ softmax / epilogue
-    // Softmax warpgroup grp handles query heads [hbase, hbase + HPG) of the
-    // group, in chunks of CH: its own maxima, probabilities, P rows, O columns
-    // and output rows, with its own named barrier.  Heads are independent, so
-    // the warpgroups never wait for each other.
-    constexpr int HPG = NPAD / GROUPS;
-    constexpr int CH = HPG % 16 == 0 ? 16 : 8;
-    constexpr int NCH = HPG / CH;
+    // Softmax warpgroup grp handles the 16 columns [hbase, hbase + 16) of
+    // S and O (query heads for decode, (query, head) pairs for prefill):
+    // their probabilities, P rows, O columns and output rows, with its own
+    // named barrier.  Columns are independent, so the warpgroups never wait
+    // for each other.
+    //
+    // Reference maxima: the exponentials of a tile use the running reference
+    // m_run of each column, p = 2^(x - m_run).  A tile only moves m_run
+    // (cross-thread maxima, rescale factor alpha, a second barrier) when one
+    // of its logits passes m_run + kHeadroom, which after the first tile of
+    // a unit is rare, so p stays below 2^kHeadroom and the result is the
+    // same softmax.  Padded columns hold m_run = +inf: their p is 0 and they
+    // never ask for a rescale.
+    constexpr int HPG = 16;
+    constexpr float kHeadroom = 8.f;
+    static_assert(NPAD == HPG * GROUPS, "one softmax warpgroup per 16 columns");
     const int grp = (warp - 2) >> 2;
     const int hbase = grp * HPG;
     const uint32_t bar = kSoftmaxBar + grp;
@@ -446,56 +404,86 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     const bool fused = a.fused != 0;           // one unit, merged over the cluster
     const int H = a.num_heads;
     const int group_heads = max(0, min(HPG, g - hbase));    // decode: valid heads of this warpgroup
+    // This thread's element (column hbase + hl, token row) of the K-major,
+    // 128-byte swizzled P^T operand sits at p_row ^ ((hl & 7) << 4), plus
+    // hl * 128: the swizzle XORs the 16-byte chunk index ((row & 63) >> 3)
+    // with the row's index mod 8, hbase is a multiple of 16, and bits 4..6
+    // of everything else are zero.
+    const uint32_t p_row = (uint32_t)((row >> 6) * NPAD * 128 + hbase * 128 +
+                                      (((row & 63) >> 3) << 4) + ((row & 7) << 1));
     float o_acc[HPG], l_part[HPG];
 #pragma unroll
     for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
     uint32_t j = 0;
+    uint32_t resc = 0;     // bit (tile & 1): that tile moved m_run (factors in ms.alpha)
     bool ok = true;
 
+    // o += (the tile's P V), rescaled first when the tile moved m_run.
     auto accumulate_o = [&](uint32_t jo) {
       const int b = jo & 1;
       ok = ok && mbar_wait(&ms.o_full[b], (jo >> 1) & 1);
       if (!ok) return;
       tc_fence_after();
+      float v[HPG];
+      tmem_ld16(lane_addr + 2 * NPAD + b * NPAD + hbase, v);
+      if ((resc >> b) & 1) {
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float v[CH], al[CH];
-        tmem_ld<CH>(lane_addr + 2 * NPAD + b * NPAD + hbase + c * CH, v);
+        for (int i = 0; i < HPG; i += 4) {
+          const float4 al = *reinterpret_cast<const float4*>(&ms.alpha[b][hbase + i]);
+          o_acc[i] = fmaf(o_acc[i], al.x, v[i]);
+          o_acc[i + 1] = fmaf(o_acc[i + 1], al.y, v[i + 1]);
+          o_acc[i + 2] = fmaf(o_acc[i + 2], al.z, v[i + 2]);
+          o_acc[i + 3] = fmaf(o_acc[i + 3], al.w, v[i + 3]);
+        }
+      } else {
 #pragma unroll
-        for (int i = 0; i < CH; i += 4)
-          *reinterpret_cast<float4*>(&al[i]) =
-              *reinterpret_cast<const float4*>(&ms.alpha[b][hbase + c * CH + i]);
-#pragma unroll
-        for (int i = 0; i < CH; ++i) o_acc[c * CH + i] = fmaf(o_acc[c * CH + i], al[i], v[i]);
+        for (int i = 0; i < HPG; ++i) o_acc[i] += v[i];
       }
       tc_fence_before();
     };
 
     UnitCursor cur = cursor_begin(ms.sched, a);
-    UnitInfo ui;
+    UnitInfo ui, nx;
     const bool alibi = a.alibi != nullptr;
-    while (ok && cursor_next<TT, PF>(cur, ms.sched, a, ui)) {
+    // Per-unit state of this warpgroup's columns in buffer ub: reference
+    // maxima (-inf; +inf for padded columns) and, for ALiBi or prefill, the
+    // slopes, causal limits and output rows.  The next unit's is written
+    // before the current unit's last barrier, so units need no barrier of
+    // their own to start.
+    auto setup_unit = [&](const UnitInfo& v, int ub) {
+      if (et < HPG) {
+        const int c = hbase + et;
+        const int hv = v.hk * g;
+        const int mh = PF ? max(0, min(HPG, v.nq * g - hbase)) : group_heads;
+        ms.m_run[ub][c] = et < mh ? -INFINITY : INFINITY;
+        if constexpr (PF) {
+          const int ncols = v.nq * g;
+          const int qi = c / g;
+          ms.lim[ub][c] = c < ncols ? v.pos0 + qi : -1;
+          ms.orow[ub][c] = (v.qrow0 + qi) * H + hv + (c - qi * g);
+          if (alibi) ms.slope[ub][c] = c < ncols ? a.alibi[hv + c % g] * kLog2e : 0.f;
+        } else if (alibi && et < mh) {
+          ms.slope[ub][c] = a.alibi[hv + c] * kLog2e;
+        }
+      }
+    };
+    bool have = cursor_next<TT, PF>(cur, ms.sched, a, ui);
+    if (have) setup_unit(ui, 0);
+    named_barrier(bar, kSoftmaxThreads);
+    uint32_t u = 0;                    // units done by this warpgroup
+    while (ok && have) {
+      const int ub = u & 1;
       const int h0 = ui.hk * g;
       // Valid columns of this warpgroup: decode, the group's heads; prefill,
       // the unit's (query, head) pairs c = query * g + head.
       const int my_heads = PF ? max(0, min(HPG, ui.nq * g - hbase)) : group_heads;
+      float* const m_run = ms.m_run[ub];
+      const float* const slope = ms.slope[ub];
+      const int* const lim = ms.lim[ub];
       bool unit_bad = false;
       int bad_from = 0x7fffffff;       // prefill: first token of a bad block seen so far
-      if constexpr (PF) {
-        // Last visible position and slope of each column.
-        const int ncols = ui.nq * g;
-        if (et < HPG) {
-          const int c = hbase + et;
-          ms.lim[c] = c < ncols ? ui.pos0 + c / g : -1;
-          if (alibi) ms.slope[c] = c < ncols ? a.alibi[h0 + c % g] * kLog2e : 0.f;
-        }
-        named_barrier(bar, kSoftmaxThreads);
-      } else if (alibi) {
-        if (et < my_heads) ms.slope[hbase + et] = a.alibi[h0 + hbase + et] * kLog2e;
-        named_barrier(bar, kSoftmaxThreads);
-      }
       // Every wait below is bounded; a thread that gives up keeps taking part
-      // in the group barriers, which AND the flag so the group stops together.
+      // in the group barriers, which combine the flag so the group stops together.
       for (int jl = 0; jl < ui.ntiles; ++jl, ++j) {
         const int b = j & 1, ks = j % NK, vs = j % NV;
         const int ts = ui.t0 + jl * TT;
@@ -510,90 +498,96 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
           unit_bad |= ms.k_bad[ks] >= 0;
         }
         mbar_arrive(&ms.k_empty[ks]);
-        // Tile maxima per head (logits kept in registers for the exponentials).
-        const uint32_t s_addr = lane_addr + b * NPAD + hbase;
+        // Logits of the tile in log2 units (masked: -inf).
         float xs[HPG];
-        const float pos = (float)(ts + row - (ui.L - 1));   // ALiBi distance to the query
+        tmem_ld16(lane_addr + b * NPAD + hbase, xs);
+        if constexpr (PF) {
+          // Causal mask per column: token ts + row is visible to column c
+          // when it does not pass that query's position.
+          const int t = ts + row;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          float x[CH];
-          tmem_ld<CH>(s_addr + c * CH, x);
-          if constexpr (PF) {
-            // Causal mask per column: token ts + row is visible to column i
-            // when it does not pass that query's position.
-            int lm[CH];
-            float sl[CH];
+          for (int i = 0; i < HPG; i += 4) {     // 4 columns at a time: few live registers
+            const int4 lm = *reinterpret_cast<const int4*>(&lim[hbase + i]);
+            const int l4[4] = {lm.x, lm.y, lm.z, lm.w};
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            if (alibi) *reinterpret_cast<float4*>(s4) =
+                *reinterpret_cast<const float4*>(&slope[hbase + i]);
 #pragma unroll
-            for (int i = 0; i < CH; i += 4) {
-              *reinterpret_cast<int4*>(&lm[i]) =
-                  *reinterpret_cast<const int4*>(&ms.lim[hbase + c * CH + i]);
-              *reinterpret_cast<float4*>(&sl[i]) =
-                  *reinterpret_cast<const float4*>(&ms.slope[hbase + c * CH + i]);
-            }
-            const int t = ts + row;
-#pragma unroll
-            for (int i = 0; i < CH; ++i) {
-              const float b = alibi ? sl[i] * (float)(t - lm[i]) : 0.f;
-              x[i] = t <= lm[i] ? fmaf(x[i], qscale, b) : -INFINITY;
-            }
-          } else if (alibi) {
-            float sl[CH];
-#pragma unroll
-            for (int i = 0; i < CH; i += 4)
-              *reinterpret_cast<float4*>(&sl[i]) =
-                  *reinterpret_cast<const float4*>(&ms.slope[hbase + c * CH + i]);
-#pragma unroll
-            for (int i = 0; i < CH; ++i) x[i] = valid ? fmaf(sl[i], pos, x[i] * qscale) : -INFINITY;
-          } else {
-#pragma unroll
-            for (int i = 0; i < CH; ++i) x[i] = valid ? x[i] * qscale : -INFINITY;
+            for (int k = 0; k < 4; ++k)
+              xs[i + k] = t <= l4[k] ? fmaf(xs[i + k], qscale, s4[k] * (float)(t - l4[k])) : -INFINITY;
           }
+        } else if (alibi) {
+          const float pos = (float)(ts + row - (ui.L - 1));   // ALiBi distance to the query
 #pragma unroll
-          for (int i = 0; i < CH; ++i) xs[c * CH + i] = x[i];
-          const float m = chunk_max<CH>(x, lane);
-          if (chunk_writer<CH>(lane)) ms.red[b][wq][hbase + c * CH + chunk_index<CH>(lane)] = m;
+          for (int i = 0; i < HPG; i += 4) {
+            const float4 sl = *reinterpret_cast<const float4*>(&slope[hbase + i]);
+            xs[i] = valid ? fmaf(sl.x, pos, xs[i] * qscale) : -INFINITY;
+            xs[i + 1] = valid ? fmaf(sl.y, pos, xs[i + 1] * qscale) : -INFINITY;
+            xs[i + 2] = valid ? fmaf(sl.z, pos, xs[i + 2] * qscale) : -INFINITY;
+            xs[i + 3] = valid ? fmaf(sl.w, pos, xs[i + 3] * qscale) : -INFINITY;
+          }
+        } else if (ts + TT <= ui.t1) {           // every row of the tile is attended
+#pragma unroll
+          for (int i = 0; i < HPG; ++i) xs[i] *= qscale;
+        } else {
+#pragma unroll
+          for (int i = 0; i < HPG; ++i) xs[i] = valid ? xs[i] * qscale : -INFINITY;
         }
-        ok = named_barrier_and(bar, kSoftmaxThreads, ok);
-        if (!ok) break;
-        if (et < my_heads) {
-          const int h = hbase + et;
-          const float mt = fmaxf(fmaxf(ms.red[b][0][h], ms.red[b][1][h]),
-                                 fmaxf(ms.red[b][2][h], ms.red[b][3][h]));
-          const float m_old = ms.m_run[h];
-          const float m_new = fmaxf(m_old, mt);
-          ms.alpha[b][h] = m_new == -INFINITY ? 1.f : fast_exp2(m_old - m_new);
-          ms.m_run[h] = m_new;
+        // Does a logit pass its column's reference by more than the headroom?
+        float over = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < HPG; i += 4) {
+          const float4 mr = *reinterpret_cast<const float4*>(&m_run[hbase + i]);
+          over = fmaxf(over, fmaxf(fmaxf(xs[i] - mr.x, xs[i + 1] - mr.y),
+                                   fmaxf(xs[i + 2] - mr.z, xs[i + 3] - mr.w)));
         }
         // A unit's output may still be read from this warpgroup's P rows by
         // its bulk stores: let them finish before the rows are overwritten.
         if (leader) bulk_wait_read_all();
-        named_barrier(bar, kSoftmaxThreads);
+        if (named_barrier_or(bar, kSoftmaxThreads, over > kHeadroom || !ok)) {
+          // Rare: move the references to the tile maxima (or stop together).
+          ok = named_barrier_and(bar, kSoftmaxThreads, ok);
+          if (!ok) break;
+          const float m = warp_max16(xs, lane);
+          if ((lane & 1) == 0) ms.red[b][wq][hbase + ((lane >> 1) & 15)] = m;
+          named_barrier(bar, kSoftmaxThreads);
+          if (et < my_heads) {
+            const int h = hbase + et;
+            const float mt = fmaxf(fmaxf(ms.red[b][0][h], ms.red[b][1][h]),
+                                   fmaxf(ms.red[b][2][h], ms.red[b][3][h]));
+            const float m_old = m_run[h];
+            const float m_new = fmaxf(m_old, mt);
+            ms.alpha[b][h] = m_new == -INFINITY ? 1.f : fast_exp2(m_old - m_new);
+            m_run[h] = m_new;
+          } else if (et < HPG) {
+            ms.alpha[b][hbase + et] = 1.f;
+          }
+          named_barrier(bar, kSoftmaxThreads);
+#pragma unroll
+          for (int i = 0; i < HPG; i += 4) {
+            const float4 al = *reinterpret_cast<const float4*>(&ms.alpha[b][hbase + i]);
+            l_part[i] *= al.x;
+            l_part[i + 1] *= al.y;
+            l_part[i + 2] *= al.z;
+            l_part[i + 3] *= al.w;
+          }
+          resc |= 1u << b;
+        } else {
+          resc &= ~(1u << b);
+        }
         // Probabilities: written 16-bit into the P^T operand, summed per thread.
-        uint8_t* pb = pbuf + b * LY::QB;
+        const uint32_t pb = smem_u32(pbuf + b * LY::QB) + p_row;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          float mr[CH], al[CH];
-#pragma unroll
-          for (int i = 0; i < CH; i += 4) {
-            *reinterpret_cast<float4*>(&mr[i]) =
-                *reinterpret_cast<const float4*>(&ms.m_run[hbase + c * CH + i]);
-            *reinterpret_cast<float4*>(&al[i]) =
-                *reinterpret_cast<const float4*>(&ms.alpha[b][hbase + c * CH + i]);
-          }
-#pragma unroll
-          for (int i = 0; i < CH; i += 2) {
-            const int hl = c * CH + i;          // head within the warpgroup
-            const int h = hbase + hl;
-            const float p0 = (valid && hl < my_heads) ? fast_exp2(xs[hl] - mr[i]) : 0.f;
-            const float p1 = (valid && hl + 1 < my_heads) ? fast_exp2(xs[hl + 1] - mr[i + 1]) : 0.f;
-            l_part[hl] = fmaf(l_part[hl], al[i], p0);
-            l_part[hl + 1] = fmaf(l_part[hl + 1], al[i + 1], p1);
-            const uint32_t pk = pack2<BF16>(p0, p1);
-            if (hl < my_heads)
-              *reinterpret_cast<uint16_t*>(pb + sw128_offset(h, row, NPAD)) = (uint16_t)pk;
-            if (hl + 1 < my_heads)
-              *reinterpret_cast<uint16_t*>(pb + sw128_offset(h + 1, row, NPAD)) = (uint16_t)(pk >> 16);
-          }
+        for (int i = 0; i < HPG; i += 2) {
+          const float2 mr = *reinterpret_cast<const float2*>(&m_run[hbase + i]);
+          const float p0 = fast_exp2(xs[i] - mr.x);       // 0 for masked rows and padded columns
+          const float p1 = fast_exp2(xs[i + 1] - mr.y);
+          l_part[i] += p0;
+          l_part[i + 1] += p1;
+          const uint32_t pk = pack2<BF16>(p0, p1);
+          if (i < my_heads) st_shared_u16((pb ^ ((i & 7) << 4)) + i * 128, (uint16_t)pk);
+          if (i + 1 < my_heads)
+            st_shared_u16((pb ^ (((i + 1) & 7) << 4)) + (i + 1) * 128, (uint16_t)(pk >> 16));
         }
         // Cache slots past the sequence end inside a loaded block may hold
         // anything (NaN included): zero those V rows before P V reads them.
@@ -615,90 +609,93 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         if (jl == ui.ntiles - 1) accumulate_o(j);
       }
       // ---------------------------------------------------------- finalise unit
+      // The warpgroup's P rows are idle now (the unit's last P V has
+      // completed): four pieces of 16 x 128 bytes (2 buffers x 2 slabs) that
+      // stage its output rows -- 4 whole fp32 rows per piece for the cluster
+      // merge, or with 16-bit output 8 rows in each of the first two pieces
+      // for bulk copies.
+      auto piece = [&](int q) { return pbuf + (q >> 1) * LY::QB + (q & 1) * NPAD * 128 + hbase * 128; };
+      const bool partial = !PF && !single;     // workspace or cluster partial: unnormalised
+      const size_t unit_row = (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
+      if (partial) {
+        if (fused) {
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float v[CH];
+          for (int hl = 0; hl < HPG; ++hl)
+            if (hl < my_heads) reinterpret_cast<float*>(piece(hl >> 2))[(hl & 3) * HD + row] = o_acc[hl];
+        } else {
+          // Workspace rows straight from registers: a warp writes 128
+          // consecutive bytes of a row per store.
+          float* const wo = a.ws_o + (unit_row + hbase) * HD + row;
 #pragma unroll
-        for (int i = 0; i < CH; ++i) v[i] = l_part[c * CH + i];
-        const float t = chunk_sum<CH>(v, lane);
-        if (chunk_writer<CH>(lane)) ms.lsum[wq][hbase + c * CH + chunk_index<CH>(lane)] = t;
+          for (int hl = 0; hl < HPG; ++hl)
+            if (hl < my_heads) wo[hl * HD] = o_acc[hl];
+        }
+      }
+      const bool have_next = cursor_next<TT, PF>(cur, ms.sched, a, nx);
+      if (have_next) setup_unit(nx, ub ^ 1);
+      {
+        const float t = warp_sum16(l_part, lane);
+        if ((lane & 1) == 0) ms.lsum[wq][hbase + ((lane >> 1) & 15)] = t;
       }
       ok = named_barrier_and(bar, kSoftmaxThreads, ok);
       if (!ok) break;
-      if (et < my_heads) {
-        const int h = hbase + et;
-        const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
-        // Prefill: a column is bad when its window reaches a bad block.
-        const bool bad = PF ? ms.lim[h] >= bad_from : unit_bad;
-        ms.inv_l[h] = bad || den == 0.f ? 0.f : 1.f / den;
-        ms.sum_l[h] = bad ? -1.f : den;
-      }
-      named_barrier(bar, kSoftmaxThreads);
-      if constexpr (PF) {
-        // Column c = (query c / g, head c % g) -> out row qrow0 + c / g, head
-        // h0 + c % g; this thread writes element d = row of each column.
-#pragma unroll
-        for (int hl = 0; hl < HPG; ++hl) {
-          if (hl < my_heads) {
-            const int c = hbase + hl;
-            const int qi = c / g;
-            const size_t orow = (size_t)(ui.qrow0 + qi) * H + h0 + (c - qi * g);
-            static_cast<uint16_t*>(a.out)[orow * HD + row] =
-                (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[c], 0.f);
+      if (partial) {
+        if (et < my_heads) {
+          const int h = hbase + et;
+          const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
+          const float l = unit_bad ? -1.f : den;        // < 0 marks a bad block
+          if (fused) {
+            ms.sum_l[h] = l;
+          } else {
+            a.ws_m[unit_row + h] = m_run[h];
+            a.ws_l[unit_row + h] = l;
           }
         }
-        if (et < my_heads) ms.m_run[hbase + et] = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
-        // The next unit's column set may differ: every thread is done with
-        // this unit's lim / inv_l before they are rewritten.
-        named_barrier(bar, kSoftmaxThreads);
-        continue;
-      }
-      // Stage this warpgroup's output rows in its own P rows (idle now: the
-      // unit's last P V has completed) and write them with bulk copies.  The
-      // warpgroup's P rows are four pieces of HPG x 128 bytes (2 buffers x 2
-      // slabs); a piece holds HPG/4 whole fp32 rows of the workspace, or with
-      // 16-bit output the first two pieces hold HPG/2 output rows each.
-      const size_t unit_row = (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
-      auto piece = [&](int q) { return pbuf + (q >> 1) * LY::QB + (q & 1) * NPAD * 128 + hbase * 128; };
-      if (single) {
-        constexpr int per = HPG / 2;            // output rows per piece
-#pragma unroll
-        for (int hl = 0; hl < HPG; ++hl) {
-          if (hl < my_heads) {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(piece(hl / per)) + (hl % per) * HD + row;
-            *dst = (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[hbase + hl], 0.f);
-          }
-        }
+        if (fused) break;   // the cluster merge reads the staged partial
       } else {
-        constexpr int per = HPG / 4;            // workspace rows per piece
+        if (et < my_heads) {
+          const int h = hbase + et;
+          const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
+          // Prefill: a column is bad when its window reaches a bad block.
+          const bool bad = PF ? lim[h] >= bad_from : unit_bad;
+          ms.inv_l[h] = bad || den == 0.f ? 0.f : 1.f / den;
+        }
+        named_barrier(bar, kSoftmaxThreads);
+        if constexpr (PF) {
+          // Column c = (query c / g, head c % g): its output row is orow[c];
+          // this thread writes element d = row of each column.
+          const int* const orow = ms.orow[ub];
 #pragma unroll
-        for (int hl = 0; hl < HPG; ++hl) {
-          if (hl < my_heads) reinterpret_cast<float*>(piece(hl / per))[(hl % per) * HD + row] = o_acc[hl];
-        }
-        if (et < my_heads && !fused) {
-          a.ws_m[unit_row + hbase + et] = ms.m_run[hbase + et];
-          a.ws_l[unit_row + hbase + et] = ms.sum_l[hbase + et];
+          for (int hl = 0; hl < HPG; ++hl) {
+            if (hl < my_heads) {
+              const int c = hbase + hl;
+              static_cast<uint16_t*>(a.out)[(size_t)orow[c] * HD + row] =
+                  (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[c], 0.f);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int hl = 0; hl < HPG; ++hl) {
+            if (hl < my_heads) {
+              uint16_t* dst = reinterpret_cast<uint16_t*>(piece(hl >> 3)) + (hl & 7) * HD + row;
+              *dst = (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[hbase + hl], 0.f);
+            }
+          }
+          fence_proxy_async_smem();
+          named_barrier(bar, kSoftmaxThreads);
+          if (leader) {
+            for (int q = 0; q * 8 < my_heads; ++q)
+              bulk_store(static_cast<char*>(a.out) + ((size_t)ui.s * H + h0 + hbase + q * 8) * HD * 2,
+                         piece(q), (uint32_t)(min(8, my_heads - q * 8) * HD * 2));
+            bulk_commit();          // waited for before this warpgroup's next P rows
+          }
         }
       }
-      fence_proxy_async_smem();
-      named_barrier(bar, kSoftmaxThreads);
-      if (fused) break;   // the cluster merge reads the staged partial
-      if (leader) {
-        const int per = single ? HPG / 2 : HPG / 4;
-        const int esz = single ? 2 : 4;
-        for (int q = 0; q * per < my_heads; ++q) {
-          const int n = min(per, my_heads - q * per);
-          const size_t r0 = single ? (size_t)ui.s * H + h0 + hbase + q * per : unit_row + hbase + q * per;
-          char* dst = single ? reinterpret_cast<char*>(a.out) : reinterpret_cast<char*>(a.ws_o);
-          bulk_store(dst + r0 * HD * esz, piece(q), (uint32_t)(n * HD * esz));
-        }
-        bulk_commit();          // waited for before this warpgroup's next P rows
-      }
-      if (et < my_heads) ms.m_run[hbase + et] = -INFINITY;
 #pragma unroll
       for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
+      ui = nx;
+      have = have_next;
+      ++u;
     }
     if (!ok && leader) set_abort(ms, a.status);
   }
@@ -742,7 +739,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r) {
         if (r < np) {
-          m[r] = ld_dsmem(dsmem_addr(&ms.m_run[h], r));
+          m[r] = ld_dsmem(dsmem_addr(&ms.m_run[0][h], r));
           l[r] = ld_dsmem(dsmem_addr(&ms.sum_l[h], r));
           M = fmaxf(M, m[r]);
           bad |= l[r] < 0.f;

@@ -96,11 +96,14 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
 struct UnitCursor {
   long long next, end;
   bool dense;
+  int s, hk, p, np;   // dense: position of the last unit returned (np < 0: none yet)
 };
 
 __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
   UnitCursor c;
   c.dense = !a.fused && a.num_seqs <= kSchedMax;
+  c.s = c.hk = c.p = 0;
+  c.np = -1;
   if (a.fused) {
     // Cluster launch: grid (P, S * Hk), one unit per CTA, partition = x.
     c.next = (long long)blockIdx.y * a.num_partitions + blockIdx.x;
@@ -123,17 +126,32 @@ __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
   if (c.dense) {
     if (c.next >= c.end) return false;
     const int j = (int)c.next++;
-    int lo = 0, hi = a.num_seqs - 1;   // last s with pre[s] <= j
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (sc.pre[mid] <= j) lo = mid; else hi = mid - 1;
+    if (c.np < 0) {
+      // First unit: binary search for the last s with pre[s] <= j.
+      int lo = 0, hi = a.num_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sc.pre[mid] <= j) lo = mid; else hi = mid - 1;
+      }
+      c.s = lo;
+      c.np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;   // units per KV head
+      const int r = j - sc.pre[lo];
+      c.hk = r / c.np;
+      c.p = r - c.hk * c.np;
+    } else if (++c.p == c.np) {
+      // Later units follow in (sequence, KV head, partition) order; sequences
+      // without units have pre[s + 1] == pre[s] and are stepped over.
+      c.p = 0;
+      if (++c.hk == a.num_kv_heads) {
+        c.hk = 0;
+        do { ++c.s; } while (sc.pre[c.s + 1] == sc.pre[c.s]);
+        c.np = (sc.pre[c.s + 1] - sc.pre[c.s]) / a.num_kv_heads;
+      }
     }
-    ui.s = lo;
-    ui.L = sc.L[lo];
-    const int np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;   // units per KV head
-    const int r = j - sc.pre[lo];
-    ui.hk = r / np;
-    ui.p = r - ui.hk * np;
+    ui.s = c.s;
+    ui.L = sc.L[c.s];
+    ui.hk = c.hk;
+    ui.p = c.p;
     ui.lok = true;
     if constexpr (PF) {
       prefill_unit<TT>(a, ui);

@@ -262,6 +262,27 @@ def decode_configs():
     return out
 
 
+def prefill_configs():
+    """Prefill workloads as {name: kwargs for make_prefill_case}: the 128-token
+    prompts of the end-to-end throughput runs in "[Performance] Support
+    MQA/GQA in decode phase by using FlashAttention" (7B models with 32 MHA
+    heads), and 64/8-head GQA chunks with and without a long cached prefix."""
+    return {
+        "prefill_mha32_prompt128_b16": dict(
+            seed=6000, num_seqs=16, num_heads=32, num_kv_heads=32, head_size=128, block_size=16,
+            num_blocks=16 * 128 // 16 + 8, context_lens=[128] * 16, query_lens=[128] * 16,
+            dtype="fp16"),
+        "prefill_gqa_prompt1024_b8": dict(
+            seed=6001, num_seqs=8, num_heads=64, num_kv_heads=8, head_size=128, block_size=16,
+            num_blocks=8 * 1024 // 16 + 8, context_lens=[1024] * 8, query_lens=[1024] * 8,
+            dtype="bf16"),
+        "prefill_gqa_chunk256_ctx4096_b4": dict(
+            seed=6002, num_seqs=4, num_heads=64, num_kv_heads=8, head_size=128, block_size=16,
+            num_blocks=4 * 4096 // 16 + 8, context_lens=[4096] * 4, query_lens=[256] * 4,
+            dtype="bf16"),
+    }
+
+
 def gather_sweep():
     """gather_cached_kv workloads as {name: kwargs for make_gather_case}."""
     return {f"gather_t{t}": dict(seed=2100 + i, num_tokens=t, num_heads=40, head_size=128,
