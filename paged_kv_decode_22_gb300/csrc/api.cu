@@ -285,7 +285,7 @@ pkd_status pkd_paged_prefill_attention(void* out, const void* q, const void* key
   if (!pkd::tma_available()) return PKD_ERR_UNSUPPORTED;
   if (num_query_tokens == 0 || max_query_len == 0) return PKD_OK;   // no query rows
 
-  const int qt = pkd::prefill_tc_queries_per_unit(g);
+  const int qt = pkd::prefill_rows_queries_per_unit(g);
   const long long tiles = ((long long)max_query_len + qt - 1) / qt;
   if (tiles > 65535) return PKD_ERR_SHAPE;
   pkd::DecodeArgs a = {};
@@ -313,7 +313,7 @@ pkd_status pkd_paged_prefill_attention(void* out, const void* q, const void* key
   a.max_query_len = max_query_len;
   a.num_q_tokens = num_query_tokens;
   a.status = device_status;
-  cudaError_t e = pkd::launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = pkd::launch_prefill_rows(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKD_OK : cuda_fail(e, "prefill launch");
 }
 

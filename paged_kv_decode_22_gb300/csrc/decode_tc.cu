@@ -79,7 +79,7 @@ struct SmemLayout {
   static constexpr int off_q = off_v + NV * TILE_BYTES;
   static constexpr int off_p = off_q + 2 * QB;
   static constexpr int off_misc = off_p + 2 * QB;
-  static constexpr int misc_bytes = 14848;
+  static constexpr int misc_bytes = 13824;
   static constexpr int bytes = off_misc + misc_bytes;
 };
 
@@ -95,8 +95,6 @@ struct Misc {
   float lsum[4][64];            // per-warp exponent sums at finalisation
   alignas(16) float inv_l[64];       // 1 / sum (0 for a bad unit)
   alignas(16) float slope[2][64];    // ALiBi slopes of the unit's columns (log2 units)
-  alignas(16) int lim[2][64];        // prefill: last visible position of each column (-1: none)
-  int orow[2][64];                   // prefill: output row (token * H + head) of each column
   float sum_l[64];                   // sum written to the workspace
   SchedSmem sched;                   // work-unit schedule
 };
@@ -144,7 +142,7 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
   return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
 }
 
-template <bool BF16, int NPAD, bool PF>
+template <bool BF16, int NPAD>
 __global__ void __launch_bounds__(threads_of(NPAD), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -238,7 +236,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     };
     UnitCursor cur = cursor_begin(ms.sched, a);
     UnitInfo ui;
-    bool have = cursor_next<TT, PF>(cur, ms.sched, a, ui);
+    bool have = cursor_next<TT>(cur, ms.sched, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -248,7 +246,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       bool nhave = true;
       int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nhave = cursor_next<TT, PF>(cur, ms.sched, a, nui);
+        nhave = cursor_next<TT>(cur, ms.sched, a, nui);
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
@@ -256,19 +254,10 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         const int qb = un & 1;
         ok = mbar_wait(&ms.q_empty[qb], ((un >> 1) & 1) ^ 1);
         if (ok) {
-          if constexpr (PF) {
-            // Chunk queries [qrow0, qrow0 + QT) x the group's g heads: rows
-            // (query, head) of the q operand, box {64, g, QT}.
-            mbar_arrive_expect_tx(&ms.q_full[qb], (uint32_t)(g * a.q_per_unit * 256));
-            tma_load_3d(qbuf + qb * LY::QB, &qmap, &ms.q_full[qb], 0, ui.hk * g, ui.qrow0);
-            tma_load_3d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, ui.hk * g,
-                        ui.qrow0);
-          } else {
-            mbar_arrive_expect_tx(&ms.q_full[qb], LY::QB);
-            const int row0 = ui.s * a.num_heads + ui.hk * g;
-            tma_load_2d(qbuf + qb * LY::QB, &qmap, &ms.q_full[qb], 0, row0);
-            tma_load_2d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, row0);
-          }
+          mbar_arrive_expect_tx(&ms.q_full[qb], LY::QB);
+          const int row0 = ui.s * a.num_heads + ui.hk * g;
+          tma_load_2d(qbuf + qb * LY::QB, &qmap, &ms.q_full[qb], 0, row0);
+          tma_load_2d(qbuf + qb * LY::QB + NPAD * 128, &qmap, &ms.q_full[qb], 64, row0);
         }
       }
       const int ts = ui.t0 + jl * TT;
@@ -335,7 +324,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       };
       UnitCursor cur = cursor_begin(ms.sched, a);
       UnitInfo ui;
-      while (ok && cursor_next<TT, PF>(cur, ms.sched, a, ui)) {
+      while (ok && cursor_next<TT>(cur, ms.sched, a, ui)) {
         // The softmax warps finish the previous unit only after its last P V:
         // issue that one before this unit's first S.
         if (prev >= 0) {
@@ -376,8 +365,8 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   } else {
     // ============================================================ softmax / epilogue
     // Softmax warpgroup grp handles the 16 columns [hbase, hbase + 16) of
-    // S and O (query heads for decode, (query, head) pairs for prefill):
-    // their probabilities, P rows, O columns and output rows, with its own
+    // S and O (query heads of the group): their probabilities, P rows, O
+    // columns and output rows, with its own
     // named barrier.  Columns are independent, so the warpgroups never wait
     // for each other.
     //
@@ -446,42 +435,27 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     UnitInfo ui, nx;
     const bool alibi = a.alibi != nullptr;
     // Per-unit state of this warpgroup's columns in buffer ub: reference
-    // maxima (-inf; +inf for padded columns) and, for ALiBi or prefill, the
-    // slopes, causal limits and output rows.  The next unit's is written
-    // before the current unit's last barrier, so units need no barrier of
-    // their own to start.
+    // maxima (-inf; +inf for padded columns) and ALiBi slopes.  The next
+    // unit's is written before the current unit's last barrier, so units
+    // need no barrier of their own to start.
     auto setup_unit = [&](const UnitInfo& v, int ub) {
       if (et < HPG) {
         const int c = hbase + et;
-        const int hv = v.hk * g;
-        const int mh = PF ? max(0, min(HPG, v.nq * g - hbase)) : group_heads;
-        ms.m_run[ub][c] = et < mh ? -INFINITY : INFINITY;
-        if constexpr (PF) {
-          const int ncols = v.nq * g;
-          const int qi = c / g;
-          ms.lim[ub][c] = c < ncols ? v.pos0 + qi : -1;
-          ms.orow[ub][c] = (v.qrow0 + qi) * H + hv + (c - qi * g);
-          if (alibi) ms.slope[ub][c] = c < ncols ? a.alibi[hv + c % g] * kLog2e : 0.f;
-        } else if (alibi && et < mh) {
-          ms.slope[ub][c] = a.alibi[hv + c] * kLog2e;
-        }
+        ms.m_run[ub][c] = et < group_heads ? -INFINITY : INFINITY;
+        if (alibi && et < group_heads) ms.slope[ub][c] = a.alibi[v.hk * g + c] * kLog2e;
       }
     };
-    bool have = cursor_next<TT, PF>(cur, ms.sched, a, ui);
+    bool have = cursor_next<TT>(cur, ms.sched, a, ui);
     if (have) setup_unit(ui, 0);
     named_barrier(bar, kSoftmaxThreads);
     uint32_t u = 0;                    // units done by this warpgroup
     while (ok && have) {
       const int ub = u & 1;
       const int h0 = ui.hk * g;
-      // Valid columns of this warpgroup: decode, the group's heads; prefill,
-      // the unit's (query, head) pairs c = query * g + head.
-      const int my_heads = PF ? max(0, min(HPG, ui.nq * g - hbase)) : group_heads;
+      const int my_heads = group_heads;   // valid columns of this warpgroup
       float* const m_run = ms.m_run[ub];
       const float* const slope = ms.slope[ub];
-      const int* const lim = ms.lim[ub];
       bool unit_bad = false;
-      int bad_from = 0x7fffffff;       // prefill: first token of a bad block seen so far
       // Every wait below is bounded; a thread that gives up keeps taking part
       // in the group barriers, which combine the flag so the group stops together.
       for (int jl = 0; jl < ui.ntiles; ++jl, ++j) {
@@ -491,32 +465,12 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         ok = ok && mbar_wait(&ms.s_full[b], (j >> 1) & 1);
         ok = ok && mbar_wait(&ms.k_full[ks], (j / NK) & 1);
         tc_fence_after();
-        if constexpr (PF) {
-          const int kb = ms.k_bad[ks];
-          if (kb >= 0) bad_from = min(bad_from, ts + kb);
-        } else {
-          unit_bad |= ms.k_bad[ks] >= 0;
-        }
+        unit_bad |= ms.k_bad[ks] >= 0;
         mbar_arrive(&ms.k_empty[ks]);
         // Logits of the tile in log2 units (masked: -inf).
         float xs[HPG];
         tmem_ld16(lane_addr + b * NPAD + hbase, xs);
-        if constexpr (PF) {
-          // Causal mask per column: token ts + row is visible to column c
-          // when it does not pass that query's position.
-          const int t = ts + row;
-#pragma unroll
-          for (int i = 0; i < HPG; i += 4) {     // 4 columns at a time: few live registers
-            const int4 lm = *reinterpret_cast<const int4*>(&lim[hbase + i]);
-            const int l4[4] = {lm.x, lm.y, lm.z, lm.w};
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-            if (alibi) *reinterpret_cast<float4*>(s4) =
-                *reinterpret_cast<const float4*>(&slope[hbase + i]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              xs[i + k] = t <= l4[k] ? fmaf(xs[i + k], qscale, s4[k] * (float)(t - l4[k])) : -INFINITY;
-          }
-        } else if (alibi) {
+        if (alibi) {
           const float pos = (float)(ts + row - (ui.L - 1));   // ALiBi distance to the query
 #pragma unroll
           for (int i = 0; i < HPG; i += 4) {
@@ -615,7 +569,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       // merge, or with 16-bit output 8 rows in each of the first two pieces
       // for bulk copies.
       auto piece = [&](int q) { return pbuf + (q >> 1) * LY::QB + (q & 1) * NPAD * 128 + hbase * 128; };
-      const bool partial = !PF && !single;     // workspace or cluster partial: unnormalised
+      const bool partial = !single;            // workspace or cluster partial: unnormalised
       const size_t unit_row = (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
       if (partial) {
         if (fused) {
@@ -631,7 +585,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
             if (hl < my_heads) wo[hl * HD] = o_acc[hl];
         }
       }
-      const bool have_next = cursor_next<TT, PF>(cur, ms.sched, a, nx);
+      const bool have_next = cursor_next<TT>(cur, ms.sched, a, nx);
       if (have_next) setup_unit(nx, ub ^ 1);
       {
         const float t = warp_sum16(l_part, lane);
@@ -656,24 +610,10 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         if (et < my_heads) {
           const int h = hbase + et;
           const float den = ms.lsum[0][h] + ms.lsum[1][h] + ms.lsum[2][h] + ms.lsum[3][h];
-          // Prefill: a column is bad when its window reaches a bad block.
-          const bool bad = PF ? lim[h] >= bad_from : unit_bad;
-          ms.inv_l[h] = bad || den == 0.f ? 0.f : 1.f / den;
+          ms.inv_l[h] = unit_bad || den == 0.f ? 0.f : 1.f / den;
         }
         named_barrier(bar, kSoftmaxThreads);
-        if constexpr (PF) {
-          // Column c = (query c / g, head c % g): its output row is orow[c];
-          // this thread writes element d = row of each column.
-          const int* const orow = ms.orow[ub];
-#pragma unroll
-          for (int hl = 0; hl < HPG; ++hl) {
-            if (hl < my_heads) {
-              const int c = hbase + hl;
-              static_cast<uint16_t*>(a.out)[(size_t)orow[c] * HD + row] =
-                  (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[c], 0.f);
-            }
-          }
-        } else {
+        {
 #pragma unroll
           for (int hl = 0; hl < HPG; ++hl) {
             if (hl < my_heads) {
@@ -778,7 +718,7 @@ int pad_group(int g) { return (g + 15) / 16 * 16; }
 
 // Kernel attributes, set once per device: the dynamic shared memory and
 // clusters of up to 16 CTAs.
-template <bool BF16, int NPAD, bool PF = false>
+template <bool BF16, int NPAD>
 cudaError_t prepare(int* smem_out) {
   const int smem = SmemLayout<NPAD>::bytes + 1024;
   *smem_out = smem;
@@ -787,9 +727,9 @@ cudaError_t prepare(int* smem_out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || attr_set[dev]) return cudaSuccess;
-  if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD, PF>,
+  if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD, PF>,
+      (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
     return e;
   attr_set[dev] = true;
@@ -831,38 +771,15 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
     cudaLaunchAttribute attr[2];
     cluster_config(&cfg, attr, dim3(a.num_partitions, a.num_seqs * a.num_kv_heads),
                    threads_of(NPAD), smem, a.num_partitions, st);
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BF16, NPAD, false>, km, vm, qm, a);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BF16, NPAD>, km, vm, qm, a);
   }
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   const int grid = (int)(units < sms ? units : sms);
-  return launch_pdl(decode_tc_kernel<BF16, NPAD, false>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
+  return launch_pdl(decode_tc_kernel<BF16, NPAD>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
                     km, vm, qm, a);
-}
-
-// Prefill: persistent grid over (sequence, KV head, query tile) units.
-template <bool BF16, int NPAD>
-cudaError_t launch_pf(const DecodeArgs& a, cudaStream_t st) {
-  CUtensorMap km, vm, qm;
-  const long long rows = (long long)a.num_blocks * a.block_size;
-  const int box_rows = a.block_size < TT ? a.block_size : TT;
-  const int g = a.num_heads / a.num_kv_heads;
-  if (!make_kv_map(&km, a.key_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
-      !make_kv_map(&vm, a.value_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
-      !make_q_chunk_map(&qm, a.q, BF16, HD, a.num_heads, a.num_q_tokens, g, a.q_per_unit))
-    return cudaErrorInvalidValue;
-  int smem = 0;
-  cudaError_t e = prepare<BF16, NPAD, true>(&smem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
-  const int grid = (int)(units < sms ? units : sms);
-  return launch_pdl(decode_tc_kernel<BF16, NPAD, true>, dim3(grid), dim3(threads_of(NPAD)), smem,
-                    st, km, vm, qm, a);
 }
 
 // Co-resident clusters of `cluster` CTAs, cached per device and cluster size.
@@ -878,7 +795,7 @@ int capacity_t(int cluster) {
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr[2];
       cluster_config(&cfg, attr, dim3(cluster), threads_of(NPAD), smem, cluster, nullptr);
-      if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<true, NPAD, false>, &cfg) !=
+      if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<true, NPAD>, &cfg) !=
           cudaSuccess) {
         cudaGetLastError();   // a refused query only means "no cluster launch"
         n = 0;
@@ -907,17 +824,6 @@ bool decode_tc_supported(int head_size, int group, int block_size) {
 }
 
 int decode_tc_tile() { return TT; }
-
-int prefill_tc_queries_per_unit(int group) { return group >= 1 && group <= 64 ? 64 / group : 0; }
-
-cudaError_t launch_prefill_tc(const DecodeArgs& a, cudaStream_t st) {
-  const int g = a.num_heads / a.num_kv_heads;
-  if (a.head_size != HD || a.q_per_unit != prefill_tc_queries_per_unit(g)) return cudaErrorInvalidValue;
-  const int cols = pad_group(g * a.q_per_unit);
-  if (cols == 48) return a.is_bf16 ? launch_pf<true, 48>(a, st) : launch_pf<false, 48>(a, st);
-  if (cols == 64) return a.is_bf16 ? launch_pf<true, 64>(a, st) : launch_pf<false, 64>(a, st);
-  return cudaErrorNotSupported;
-}
 
 int decode_tc_cluster_capacity(int group, int cluster) {
   if (cluster < 2 || cluster > kMaxCluster || group < 4 || group > 64) return 0;

@@ -94,10 +94,10 @@ int decode_tc_tile();
 // Clusters of `cluster` CTAs of the tensor-core kernel for query-group size
 // `group` that the current device holds at once (0: cannot launch).
 int decode_tc_cluster_capacity(int group, int cluster);
-// Prefill on the tensor-core kernel: query tokens per work unit for a
-// query-group size (their columns fill at most 64 MMA columns), and the launch.
-int prefill_tc_queries_per_unit(int group);
-cudaError_t launch_prefill_tc(const DecodeArgs& a, cudaStream_t st);
+// Prefill on the row-per-thread tensor-core kernel (128 (query, head) rows
+// per unit, S and O in TMEM): query tokens per unit and the launch.
+int prefill_rows_queries_per_unit(int group);
+cudaError_t launch_prefill_rows(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st);
