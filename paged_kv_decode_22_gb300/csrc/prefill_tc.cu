@@ -320,19 +320,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) x[c * 32 + i] = v[i];
         }
-        if (ts + TT - 1 <= pos && !alibi) {
-#pragma unroll
-          for (int i = 0; i < TT; ++i) x[i] *= qscale;
-        } else {
+        // Logits in log2 units are x * sc: without ALiBi the scale folds into
+        // the exponent's FMA (sc = scale * log2 e > 0: the maximum of x is the
+        // maximum of the logits); with ALiBi x carries the scale and the bias.
+        const bool fold = !alibi && qscale > 0.f;
+        const float sc = fold ? qscale : 1.f;
+        if (!fold) {
 #pragma unroll
           for (int i = 0; i < TT; ++i) {
             const int t = ts + i;
             x[i] = t <= pos ? fmaf(x[i], qscale, slope * (float)(t - pos)) : -INFINITY;
           }
-        }
-        float mx = x[0];
+        } else if (ts + TT - 1 > pos) {         // the tile passes this row's query
 #pragma unroll
-        for (int i = 1; i < TT; ++i) mx = fmaxf(mx, x[i]);
+          for (int i = 0; i < TT; ++i) x[i] = ts + i <= pos ? x[i] : -INFINITY;
+        }
+        // Row maximum: 8 independent chains, then a 3-level tree.
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+        for (int i = 8; i < TT; i += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], x[i + k]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sc;
         float alpha = 1.f;
         if (mx > m_ref + kHeadroom) {
           const float m_new = fmaxf(m_ref, mx);
@@ -358,21 +370,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // P = 2^(x - m_ref), 16-bit pairs over the S buffer's first 64 columns.
-        float lt = 0.f;
+        // P = 2^(x * sc - m_ref), 16-bit pairs over the S buffer's first 64
+        // columns; the row sum in 8 independent chains.
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t w[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(x[c * 64 + 2 * i] - m_ref);
-            const float p1 = fast_exp2(x[c * 64 + 2 * i + 1] - m_ref);
-            lt += p0 + p1;
+            const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sc, -m_ref));
+            const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sc, -m_ref));
+            l8[(2 * i) & 7] += p0;
+            l8[(2 * i + 1) & 7] += p1;
             w[i] = pack2<BF16>(p0, p1);
           }
           tmem_st32(lane_addr + b * 128 + c * 32, w);
         }
-        l += lt;
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
         // Cache slots past the sequence end inside a loaded block may hold
         // anything (NaN included): zero those V rows before P V reads them
         // (thread `row` clears token row `row` of the tile).
