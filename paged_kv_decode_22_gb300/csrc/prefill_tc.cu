@@ -9,7 +9,7 @@
 // 128 rows are the (query, head) pairs r = query * g + head, so all g heads
 // of a query share every K/V tile.  A persistent grid of one CTA per SM walks
 // the units (the shared schedule of the decode kernel); inside the CTA:
-//   warp 0     K producer (and the unit's Q tile): TMA boxes of one block x
+//   warps 0, 3 K producers (half 0 and the unit's Q tile; half 1): TMA boxes of one block x
 //              64 columns into a ring of 32 KB stages, block ids one tile
 //              ahead, out-of-range blocks from an out-of-bounds row (zeros).
 //   warp 1     V producer, same boxes into its own ring.
@@ -127,9 +127,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ms.tmem_base;
 
-  if (warp == 0 || warp == 1) {
+  if (warp == 0 || warp == 1 || warp == 3) {
     // ============================================================ producers
+    // Warp 0 issues K's first 64-column half (and owns the stage's barrier
+    // bookkeeping and the Q loads), warp 3 K's second half in parallel, warp
+    // 1 both halves of V.
     const bool is_v = warp == 1;
+    const bool primary = warp != 3;
+    const int half_mask = warp == 0 ? 1 : warp == 3 ? 2 : 3;
     const int B = a.block_size;
     const int R = B < TT ? B : TT;            // rows per TMA box
     const int nbox = TT / R;                  // boxes per tile and 64-column half
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nst = is_v ? NV : NK;
     uint64_t* full = is_v ? ms.v_full : ms.k_full;
     uint64_t* empty = is_v ? ms.v_empty : ms.k_empty;
-    const bool issuer = lane < 2 * nbox;
+    const bool issuer = lane < 2 * nbox && ((half_mask >> (lane / nbox)) & 1);
     const int my_box = lane % nbox, my_half = lane / nbox;
     auto load_raw = [&](const UnitInfo& t, int tj) {
       int raw = kNoBlock;
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
-      if (!is_v && jl == 0 && lane == 0) {
+      if (!is_v && primary && jl == 0 && lane == 0) {
         const int qb = un & 1;
         ok = mbar_wait(&ms.q_empty[qb], ((un >> 1) & 1) ^ 1);
         if (ok) {
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = jk % nst;
       if (lane == 0) {
         ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
-        if (ok) {
+        if (ok && primary) {
           if (!is_v) {
             ms.k_bad[st] = bad_lanes ? (__ffs(bad_lanes) - 1) * R : -1;
             if (bad_lanes) flag(a.status, PKD_DEV_BAD_BLOCK);
