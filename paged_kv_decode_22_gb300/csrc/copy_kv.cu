@@ -8,8 +8,9 @@
 // In the [num_blocks][block_size][num_heads][head_size] layout a slot's row
 // of num_heads * head_size elements is contiguous, so both directions are
 // plain row copies.  One CTA copies one token's K row (blockIdx.y = 0) or V
-// row (blockIdx.y = 1) with 16-byte streaming loads and stores, four in
-// flight per thread.
+// row (blockIdx.y = 1) with 16-byte streaming loads and stores, five in
+// flight per thread (a 40-head x 128 row of 640 chunks is one round of 128
+// threads).
 #include "common.cuh"
 #include "internal.h"
 
@@ -17,7 +18,7 @@ namespace pkd {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kInflight = 4;
+constexpr int kInflight = 5;
 
 __device__ __forceinline__ void copy_row(char* dst, const char* src, int n16) {
   for (int i0 = threadIdx.x; i0 < n16; i0 += kThreads * kInflight) {
