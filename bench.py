@@ -673,15 +673,29 @@ def main():
                              "path": PATH_NAMES[pathx], "partitions": npx,
                              "copies": tcopies}
 
+    # Prefill lines (tensor-bound): same method, FLOPs against the bf16 peak.
+    prefill_lines = {}
+    if not args.no_targets:
+        from paged_kv_decode_22_gb300.workloads import prefill_configs
+        for name in prefill_configs():
+            us, flops, nbytes, pcopies = time_prefill_workload(name, dev, ops)
+            prefill_lines[name] = {"us_per_call": round(us, 2), "TFLOPs": round(flops / us / 1e6, 1),
+                                   "GBps": round(nbytes / us / 1e3, 1), "copies": pcopies}
+
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    tpeak = FALLBACK_BF16_TFLOPS
     if os.path.exists(peaks_path):
         with open(peaks_path) as f:
             pk = json.load(f)
         if pk.get("hbm_gbs"):
             peak, peak_src = float(pk["hbm_gbs"]), "measured"
+        if pk.get("bf16_tflops"):
+            tpeak = float(pk["bf16_tflops"])
     for v in targets.values():
         v["frac"] = round(v["GBps"] / peak, 3)
+    for v in prefill_lines.values():
+        v["frac_tensor"] = round(v["TFLOPs"] / tpeak, 3)
 
     if rank != 0:
         if dist is not None:
@@ -717,6 +731,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
         "targets_decode_bf16_gqa64x8": targets,
+        "targets_prefill": prefill_lines,
     }
     if world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(c, g)
