@@ -77,7 +77,9 @@ template <int TT, bool PF>
 __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
   UnitInfo ui;
   const int P = a.num_partitions;
-  ui.p = u % P;
+  // Prefill: a sequence's later query tiles see more of the cache, so they
+  // are dealt first (heaviest units first, light ones fill the tail).
+  ui.p = PF ? P - 1 - u % P : u % P;
   const int sh = u / P;
   ui.hk = sh % a.num_kv_heads;
   ui.s = sh / a.num_kv_heads;
@@ -101,7 +103,9 @@ struct UnitCursor {
 
 __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
   UnitCursor c;
-  c.dense = !a.fused && a.num_seqs <= kSchedMax;
+  // Prefill takes units round-robin: consecutive query tiles of a causal
+  // chunk differ in cost, and dealing them across CTAs balances it.
+  c.dense = !a.fused && !a.query_start && a.num_seqs <= kSchedMax;
   c.s = c.hk = c.p = 0;
   c.np = -1;
   if (a.fused) {
