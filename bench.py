@@ -40,7 +40,7 @@ WORKLOAD = "llama13b_mha_b8_ctx256 decode + gather_t2048"
 DECODE_CFG = "llama13b_mha_b8_ctx256"
 GATHER_CFG = "gather_t2048"
 TARGETS = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "gqa_ctx4096_b256"]
-PATH_NAMES = {0: "simt", 1: "tc", 2: "tc_cluster"}   # decode_plan's kernel family
+PATH_NAMES = {0: "simt", 1: "tc", 2: "tc_cluster", 3: "tc_stream"}   # decode_plan's kernel family
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -264,9 +264,10 @@ def graph_time(fns, calls=32, reps=5):
     return e0.elapsed_time(e1) * 1e3 / (reps * calls)
 
 
-def time_decode_workload(name, dev, ops):
+def time_decode_workload(name, dev, ops, partition_size=0):
     """(us per call, algorithmic bytes, plan) of one decode workload, inputs
-    rotated over enough copies to exceed 3x L2."""
+    rotated over enough copies to exceed 3x L2; partition_size as in
+    paged_decode_attention (0: the library's plan)."""
     import torch
     d0 = device_decode_inputs(name, dev)
     S, H, D = d0["q"].shape
@@ -274,10 +275,11 @@ def time_decode_workload(name, dev, ops):
     ncopy = max(1, min(8, math.ceil(3 * L2_BYTES / d0["bytes"])))
     sets = [d0] + [dict(d0, q=d0["q"].clone(), kc=d0["kc"].clone(), vc=d0["vc"].clone(),
                         out=torch.empty_like(d0["out"])) for _ in range(ncopy - 1)]
-    plan = ops.decode_plan(S, H, Hk, D, B, d0["max_ctx"])
+    plan = ops.decode_plan(S, H, Hk, D, B, d0["max_ctx"], partition_size)
     work = torch.empty(max(plan[3], 256), dtype=torch.uint8, device=dev)
     fns = [lambda d=d: ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"],
                                                   d["cl"], d["max_ctx"], d["scale"],
+                                                  partition_size=partition_size,
                                                   workspace=work) for d in sets]
     us = graph_time(fns)
     nbytes = d0["bytes"]
@@ -395,12 +397,13 @@ def run_profile(args, local):
         d = device_decode_inputs(name, dev)
         S, H, D = d["q"].shape
         _, npart, _, ws = ops.decode_plan(S, H, d["kc"].shape[2], D, d["kc"].shape[1],
-                                          d["max_ctx"])
+                                          d["max_ctx"], args.partition_size)
         work = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
 
         def call():
             ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"], d["cl"],
-                                       d["max_ctx"], d["scale"], workspace=work)
+                                       d["max_ctx"], d["scale"], workspace=work,
+                                       partition_size=args.partition_size)
     elif kind == "prefill":
         d = device_prefill_inputs(name, dev)
 
@@ -447,7 +450,12 @@ def run_sweep(args, local):
         with open(pk_path) as f:
             peak = float(json.load(f).get("hbm_gbs") or peak)
     for name in decode_configs():
-        us, nbytes, (ps, npart, path, _), ncopy = time_decode_workload(name, dev, ops)
+        try:
+            us, nbytes, (ps, npart, path, _), ncopy = time_decode_workload(
+                name, dev, ops, args.partition_size)
+        except ops.PkdError as e:        # a forced partition size this workload cannot take
+            print(json.dumps({"workload": name, "kind": "decode", "skipped": str(e)}), flush=True)
+            continue
         print(json.dumps({"workload": name, "kind": "decode", "us_per_call": round(us, 2),
                           "GBps": round(nbytes / us / 1e3, 1),
                           "frac": round(nbytes / us / 1e3 / peak, 3),
@@ -499,6 +507,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--sweep", action="store_true",
                     help="time every decode workload and gather point (one JSON line each)")
+    ap.add_argument("--partition-size", type=int, default=0,
+                    help="--sweep/--profile decode lines: forced partition_size "
+                         "(0 = the library's plan, -1 = the stream form)")
     ap.add_argument("--profile", default=None, metavar="KIND:NAME",
                     help="profiling mode: run only 'decode:<workload>', 'prefill:<workload>' or "
                          "'gather:<workload>' "

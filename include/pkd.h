@@ -89,19 +89,32 @@ typedef enum pkd_dtype { PKD_FP16 = 0, PKD_BF16 = 1 } pkd_dtype;
 #define PKD_PATH_TC 1     /* tcgen05 tensor-core path with TMA staging */
 #define PKD_PATH_TC_CLUSTER 2 /* the same, its context partitions merged inside
                                  thread-block clusters: no workspace, one launch */
+#define PKD_PATH_TC_STREAM 3  /* the tensor-core kernel in stream form: one CTA per
+                                 SM, each taking an equal contiguous share of all
+                                 128-token tiles; the (sequence, KV head) runs cut
+                                 at a share's edges are merged by a second launch */
+
+/* partition_size value that asks for the stream form (tensor-core path,
+ * num_seqs <= 1024); the call returns PKD_ERR_UNSUPPORTED where it cannot
+ * be used. */
+#define PKD_PARTITION_STREAM (-1)
 
 /*
  * Launch plan of pkd_paged_decode_attention for the given sizes on the
  * CURRENT device (same size rules as that call).  partition_size = 0 lets
  * the library choose; a positive value (a multiple of 64 tokens) forces
- * that partition length.  Outputs
+ * that partition length; PKD_PARTITION_STREAM forces the stream form, which
+ * reports a partition length of 128 and one partition.  Outputs
  * (any may be NULL): the partition length in tokens, the number of
  * partitions (1 = no split, no reduction launch), the kernel family, and the
  * workspace bytes the call needs (0 when unsplit, and for
  * PKD_PATH_TC_CLUSTER, whose split is merged inside the one launch).  The
  * tensor-core path merges a split inside thread-block clusters when it has
  * at most 16 partitions and the clusters of all (sequence, KV head) pairs fit
- * on the device at once.  Pure host arithmetic plus cached device-attribute
+ * on the device at once.  It takes the stream form (workspace: 2 partial
+ * rows per SM and query head of a group, plus the tile prefix) when that
+ * form's estimated time, which assumes every sequence at max_context_len,
+ * is lower.  Pure host arithmetic plus cached device-attribute
  * and occupancy queries; allocates nothing.
  */
 PKD_API pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
@@ -124,7 +137,8 @@ PKD_API pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads
  *   num_heads % num_kv_heads == 0;  head_size in {64, 128};
  *   block_size a power of two in [8, 256];  1 <= num_seqs <= 65535
  *   scale         logit multiplier (1/sqrt(head_size) for standard attention)
- *   partition_size  0 = library choice, else a multiple of 64 tokens
+ *   partition_size  0 = library choice, PKD_PARTITION_STREAM = stream form,
+ *                 else a multiple of 64 tokens
  *   workspace     device scratch of >= the plan's workspace bytes (may be
  *                 NULL when that is 0); its contents on entry do not matter
  *                 and are clobbered

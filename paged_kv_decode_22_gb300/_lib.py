@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libpkd.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "pkd.h")
 
 FP16, BF16 = 0, 1
-PATH_SIMT, PATH_TC, PATH_TC_CLUSTER = 0, 1, 2
+PATH_SIMT, PATH_TC, PATH_TC_CLUSTER, PATH_TC_STREAM = 0, 1, 2, 3
+PARTITION_STREAM = -1   # partition_size that asks for the stream form
 DEV_BAD_BLOCK, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8
 
 _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p

@@ -61,8 +61,9 @@ struct Plan {
   int num_partitions = 1;
   int path = PKD_PATH_SIMT;
   bool fused = false;                   // tensor-core split merged inside clusters
+  int stream_ctas = 0;                  // > 0: tensor-core stream form on that many CTAs
   size_t ws_bytes = 0;
-  size_t off_m = 0, off_l = 0;
+  size_t off_m = 0, off_l = 0, off_desc = 0;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -101,26 +102,43 @@ double tc_cluster_cost(int tiles, int P) {
   return (double)((tiles + P - 1) / P) + 0.25 + kClusterMergeCost;
 }
 
+// Stream form: every CTA takes an equal share of all tiles, at most two more
+// units than units / ctas (its range edges), and a merge launch follows.
+double tc_stream_cost(long long units, int tiles, int ctas) {
+  return (double)units * tiles / ctas + 0.25 * ((double)units / ctas + 2.0) + 2.0;
+}
+
+// The stream form builds its tile prefix in shared memory (at most 1024
+// sequences) and counts tiles in 32-bit integers.
+bool stream_fits(int num_seqs, int num_kv_heads, int max_tiles) {
+  return num_seqs <= pkd::decode_tc_sched_max() &&
+         (long long)num_seqs * num_kv_heads * max_tiles < (1LL << 30);
+}
+
 pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                      int max_context_len, int block_size, int partition_size, Plan* plan) {
   pkd_status st = check_decode_sizes(num_seqs, num_heads, num_kv_heads, head_size, max_context_len);
   if (st != PKD_OK) return st;
-  if (partition_size < 0) return PKD_ERR_SHAPE;
+  if (partition_size < PKD_PARTITION_STREAM) return PKD_ERR_SHAPE;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != PKD_OK) return st;
   const int g = num_heads / num_kv_heads;
   Plan p;
   const int tc_tile = pkd::decode_tc_tile();
   const bool tc = pkd::decode_tc_supported(head_size, g, block_size) &&
-                  (partition_size == 0 || partition_size % tc_tile == 0);
+                  (partition_size <= 0 || partition_size % tc_tile == 0);
   p.path = tc ? PKD_PATH_TC : PKD_PATH_SIMT;
   const int quantum = tc ? tc_tile : kPartitionQuantum;
   const int max_tiles = std::max(1, (max_context_len + quantum - 1) / quantum);
-  if (partition_size > 0) {
+  const long long units = (long long)num_seqs * num_kv_heads;
+  bool stream = false;
+  if (partition_size == PKD_PARTITION_STREAM) {
+    if (!tc || !stream_fits(num_seqs, num_kv_heads, max_tiles)) return PKD_ERR_UNSUPPORTED;
+    stream = true;
+  } else if (partition_size > 0) {
     if (partition_size % kPartitionQuantum) return PKD_ERR_SHAPE;
     p.partition_size = partition_size;
   } else if (tc) {
-    const long long units = (long long)num_seqs * num_kv_heads;
     int best = 1;
     double best_cost = tc_cost(units, max_tiles, 1, dev.sms);
     for (int P = 2; P <= max_tiles && P <= 64; ++P) {
@@ -132,6 +150,8 @@ pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_siz
       }
     }
     p.partition_size = ((max_tiles + best - 1) / best) * quantum;
+    stream = stream_fits(num_seqs, num_kv_heads, max_tiles) &&
+             tc_stream_cost(units, max_tiles, dev.sms) < best_cost * 0.97;
   } else {
     const long long units = (long long)num_seqs * num_kv_heads * (g / pkd::simt_heads_per_cta(g));
     const long long target = (long long)kTargetCtasPerSm * dev.sms;
@@ -139,6 +159,20 @@ pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_siz
     parts = std::min<long long>(parts, max_tiles);
     const int tiles = (int)((max_tiles + parts - 1) / parts);
     p.partition_size = tiles * quantum;
+  }
+  if (stream) {
+    // One tile per partition in the prefix; 2 partial slots and one
+    // range-edge descriptor per CTA.
+    p.partition_size = tc_tile;
+    p.num_partitions = 1;
+    p.stream_ctas = dev.sms;
+    const size_t rows = (size_t)2 * dev.sms * g;
+    p.off_m = align256(rows * head_size * sizeof(float));
+    p.off_l = p.off_m + align256(rows * sizeof(float));
+    p.off_desc = p.off_l + align256(rows * sizeof(float));
+    p.ws_bytes = p.off_desc + align256((size_t)dev.sms * sizeof(int4));
+    *plan = p;
+    return PKD_OK;
   }
   p.num_partitions = std::max(1, (max_context_len + p.partition_size - 1) / p.partition_size);
   if (p.num_partitions > 65535) return PKD_ERR_SHAPE;
@@ -168,7 +202,8 @@ pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int he
   if (st != PKD_OK) return st;
   if (out_partition_size) *out_partition_size = p.partition_size;
   if (out_num_partitions) *out_num_partitions = p.num_partitions;
-  if (out_path) *out_path = p.fused ? PKD_PATH_TC_CLUSTER : p.path;
+  if (out_path)
+    *out_path = p.fused ? PKD_PATH_TC_CLUSTER : p.stream_ctas > 0 ? PKD_PATH_TC_STREAM : p.path;
   if (out_workspace_bytes) *out_workspace_bytes = p.ws_bytes;
   return PKD_OK;
 }
@@ -238,17 +273,23 @@ pkd_status pkd_paged_decode_attention_ex(void* out, const void* q, const void* k
   a.partition_size = plan.partition_size;
   a.num_partitions = plan.num_partitions;
   a.fused = plan.fused ? 1 : 0;
+  a.stream = plan.stream_ctas > 0 ? 1 : 0;
+  a.stream_ctas = plan.stream_ctas;
   char* ws = static_cast<char*>(workspace);
   const bool use_ws = plan.ws_bytes > 0;
   a.ws_o = use_ws ? reinterpret_cast<float*>(ws) : nullptr;
   a.ws_m = use_ws ? reinterpret_cast<float*>(ws + plan.off_m) : nullptr;
   a.ws_l = use_ws ? reinterpret_cast<float*>(ws + plan.off_l) : nullptr;
+  a.ws_desc = a.stream ? reinterpret_cast<int4*>(ws + plan.off_desc) : nullptr;
   a.status = device_status;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = plan.path == PKD_PATH_TC ? pkd::launch_decode_tc(a, s) : pkd::launch_decode_simt(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (use_ws) {
+  if (a.stream) {
+    e = pkd::launch_stream_merge(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream merge launch");
+  } else if (use_ws) {
     e = pkd::launch_lse_reduce(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "lse_reduce launch");
   }

@@ -569,8 +569,13 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       // merge, or with 16-bit output 8 rows in each of the first two pieces
       // for bulk copies.
       auto piece = [&](int q) { return pbuf + (q >> 1) * LY::QB + (q & 1) * NPAD * 128 + hbase * 128; };
-      const bool partial = !single;            // workspace or cluster partial: unnormalised
-      const size_t unit_row = (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
+      // Workspace or cluster partial (unnormalised), or a whole result.  In
+      // the stream form a unit cut by the CTA's range edge is a partial in
+      // its slot; every other unit is whole.
+      const bool partial = a.stream ? ui.slot >= 0 : !single;
+      const size_t unit_row =
+          a.stream ? (size_t)ui.slot * g
+                   : (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
       if (partial) {
         if (fused) {
 #pragma unroll
@@ -777,7 +782,7 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
-  const int grid = (int)(units < sms ? units : sms);
+  const int grid = a.stream ? a.stream_ctas : (int)(units < sms ? units : sms);
   return launch_pdl(decode_tc_kernel<BF16, NPAD>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
                     km, vm, qm, a);
 }
@@ -824,6 +829,7 @@ bool decode_tc_supported(int head_size, int group, int block_size) {
 }
 
 int decode_tc_tile() { return TT; }
+int decode_tc_sched_max() { return kSchedMax; }
 
 int decode_tc_cluster_capacity(int group, int cluster) {
   if (cluster < 2 || cluster > kMaxCluster || group < 4 || group > 64) return 0;

@@ -50,6 +50,14 @@ struct DecodeArgs {
   int fused;            // tensor-core path only: the partitions of one (sequence,
                         // KV head) form one thread-block cluster and are merged
                         // through distributed shared memory (no workspace)
+  int stream;           // tensor-core path only: CTA b takes tiles [T b / G, T (b + 1) / G)
+                        // of all (sequence, KV head) pairs in order (partition_size = 128,
+                        // num_partitions = 1); a unit cut by a range edge leaves a partial
+                        // in slot 2b (the CTA's first unit) or 2b + 1 (its last)
+  int stream_ctas;      // stream: G, the grid size
+  int4* ws_desc;        // stream: [G] the (sequence, KV head) cut by the left edge of CTA
+                        // b's range, written by CTA b: {first tile A, tiles n, s * Hk + hk,
+                        // total tiles T}; n = 0 when no pair is cut there
   const int32_t* query_start;   // prefill: [S + 1] cumulative chunk lengths (nullptr: decode)
   int q_per_unit;       // prefill: query tokens per work unit
   int max_query_len;    // prefill: longer chunks are invalid (zero rows)
@@ -91,6 +99,7 @@ int simt_heads_per_cta(int group);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 bool decode_tc_supported(int head_size, int group, int block_size);
 int decode_tc_tile();
+int decode_tc_sched_max();   // sequences the in-kernel tile prefix holds
 // Clusters of `cluster` CTAs of the tensor-core kernel for query-group size
 // `group` that the current device holds at once (0: cannot launch).
 int decode_tc_cluster_capacity(int group, int cluster);
@@ -99,6 +108,7 @@ int decode_tc_cluster_capacity(int group, int cluster);
 int prefill_rows_queries_per_unit(int group);
 cudaError_t launch_prefill_rows(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_stream_merge(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st);
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st);
 

@@ -10,6 +10,10 @@
 // With more sequences CTAs take units round-robin and skip the empty ones.
 // In the cluster form of the tensor-core kernel each CTA takes the single
 // unit its grid position names (x = partition, y = sequence * Hk + KV head).
+// In the stream form the prefix counts 128-token tiles and CTA b takes the
+// tiles [T b / G, T (b + 1) / G) of the (sequence, KV head)-major tile list:
+// a unit is a run of them inside one (sequence, KV head), and only a CTA's
+// first and last units can be cut short (partials in slots 2b and 2b + 1).
 // For prefill a unit is (sequence, KV head, query tile) and reads the cache
 // from token 0 up to the position of the tile's last query.
 #pragma once
@@ -30,6 +34,7 @@ struct SchedSmem {
 struct UnitInfo {
   int s, hk, p, L, t0, t1, ntiles;
   bool lok;
+  int slot;   // stream form: workspace slot of a partial unit, -1 for a whole one
   // Prefill only: the unit's queries are chunk queries [p * QT, p * QT + nq)
   // of sequence s, stored from packed row qrow0 on; the first sits at
   // position pos0, query c at pos0 + c.
@@ -97,8 +102,9 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
 
 struct UnitCursor {
   long long next, end;
-  bool dense;
-  int s, hk, p, np;   // dense: position of the last unit returned (np < 0: none yet)
+  bool dense, first;
+  int s, hk, p, np;   // dense: position of the last unit returned (np < 0: none yet);
+                      // stream: position of the next tile (np = tiles of sequence s)
 };
 
 __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
@@ -108,7 +114,13 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
   c.dense = !a.fused && !a.query_start && a.num_seqs <= kSchedMax;
   c.s = c.hk = c.p = 0;
   c.np = -1;
-  if (a.fused) {
+  c.first = true;
+  if (a.stream) {
+    // Stream form: an equal contiguous range of the sequence-major tile list.
+    const long long total = sc.total;
+    c.next = total * blockIdx.x / gridDim.x;
+    c.end = total * (blockIdx.x + 1) / gridDim.x;
+  } else if (a.fused) {
     // Cluster launch: grid (P, S * Hk), one unit per CTA, partition = x.
     c.next = (long long)blockIdx.y * a.num_partitions + blockIdx.x;
     c.end = c.next + 1;
@@ -127,6 +139,46 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
 template <int TT, bool PF = false>
 __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
                                             const DecodeArgs& a, UnitInfo& ui) {
+  if (a.stream && !PF) {
+    // Units are the runs of the CTA's tile range inside one (sequence, KV
+    // head); pre[] counts tiles (partition_size = TT), so np = tiles of s.
+    if (c.next >= c.end) return false;
+    const int t = (int)c.next;
+    if (c.np < 0) {
+      int lo = 0, hi = a.num_seqs - 1;   // last s with pre[s] <= t
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sc.pre[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      c.s = lo;
+      c.np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;
+      const int r = t - sc.pre[lo];
+      c.hk = r / c.np;
+      c.p = r - c.hk * c.np;
+    }
+    const int off = c.p;
+    const int n = (int)min((long long)(c.np - off), c.end - c.next);
+    ui.s = c.s;
+    ui.hk = c.hk;
+    ui.p = 0;
+    ui.L = sc.L[c.s];
+    ui.lok = true;
+    ui.t0 = off * TT;
+    ui.t1 = min(ui.L, (off + n) * TT);
+    ui.ntiles = n;
+    ui.slot = (off > 0 || off + n < c.np) ? 2 * (int)blockIdx.x + (c.first ? 0 : 1) : -1;
+    c.first = false;
+    c.next += n;
+    if (c.next < c.end) {                // step to the next tile's (sequence, KV head)
+      c.p = 0;
+      if (++c.hk == a.num_kv_heads) {
+        c.hk = 0;
+        do { ++c.s; } while (sc.pre[c.s + 1] == sc.pre[c.s]);
+        c.np = (sc.pre[c.s + 1] - sc.pre[c.s]) / a.num_kv_heads;
+      }
+    }
+    return true;
+  }
   if (c.dense) {
     if (c.next >= c.end) return false;
     const int j = (int)c.next++;
@@ -206,6 +258,27 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
       if (lane == 0) {
         sc.pre[0] = 0;
         sc.total = carry;
+      }
+    }
+    if (a.stream && warp == 0) {
+      // The pair cut by this CTA's left range edge, for the merge launch
+      // (warp 0 wrote the prefix).
+      __syncwarp();
+      if (lane == 0) {
+        const long long T = sc.total;
+        const int t = (int)(T * blockIdx.x / gridDim.x);
+        int4 d = make_int4(0, 0, 0, (int)T);
+        if (blockIdx.x > 0 && t < T) {
+          int lo = 0, hi = a.num_seqs - 1;   // last s with pre[s] <= t
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sc.pre[mid] <= t) lo = mid; else hi = mid - 1;
+          }
+          const int np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;
+          const int r = t - sc.pre[lo], hk = r / np;
+          if (r - hk * np > 0) d = make_int4(sc.pre[lo] + hk * np, np, lo * a.num_kv_heads + hk, (int)T);
+        }
+        a.ws_desc[blockIdx.x] = d;
       }
     }
   }
