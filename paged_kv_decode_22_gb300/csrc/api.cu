@@ -112,7 +112,7 @@ double tc_stream_cost(long long units, int tiles, int ctas) {
 // sequences) and counts tiles in 32-bit integers.
 bool stream_fits(int num_seqs, int num_kv_heads, int max_tiles) {
   return num_seqs <= pkd::decode_tc_sched_max() &&
-         (long long)num_seqs * num_kv_heads * max_tiles < (1LL << 30);
+         (long long)num_seqs * num_kv_heads * (max_tiles + pkd::kStreamTailCost) < (1LL << 30);
 }
 
 pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
@@ -163,7 +163,7 @@ pkd_status make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_siz
   if (stream) {
     // One tile per partition in the prefix; 2 partial slots and one
     // range-edge descriptor per CTA.
-    p.partition_size = tc_tile;
+    p.partition_size = pkd::kStreamTile;
     p.num_partitions = 1;
     p.stream_ctas = dev.sms;
     const size_t rows = (size_t)2 * dev.sms * g;

@@ -49,6 +49,7 @@ namespace {
 using namespace sm100;
 
 constexpr int TT = 128;                 // tokens per tile (= MMA M for S)
+static_assert(TT == kStreamTile, "the stream form's positions are this kernel's tiles");
 constexpr int HD = 128;                 // head_size of this path (= MMA M for O)
 constexpr int TILE_BYTES = TT * HD * 2; // one K or V tile, 32 KB
 constexpr int kSoftmaxThreads = 128;   // one softmax warpgroup
@@ -495,9 +496,6 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
           over = fmaxf(over, fmaxf(fmaxf(xs[i] - mr.x, xs[i + 1] - mr.y),
                                    fmaxf(xs[i + 2] - mr.z, xs[i + 3] - mr.w)));
         }
-        // A unit's output may still be read from this warpgroup's P rows by
-        // its bulk stores: let them finish before the rows are overwritten.
-        if (leader) bulk_wait_read_all();
         if (named_barrier_or(bar, kSoftmaxThreads, over > kHeadroom || !ok)) {
           // Rare: move the references to the tile maxima (or stop together).
           ok = named_barrier_and(bar, kSoftmaxThreads, ok);
@@ -565,9 +563,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       // ---------------------------------------------------------- finalise unit
       // The warpgroup's P rows are idle now (the unit's last P V has
       // completed): four pieces of 16 x 128 bytes (2 buffers x 2 slabs) that
-      // stage its output rows -- 4 whole fp32 rows per piece for the cluster
-      // merge, or with 16-bit output 8 rows in each of the first two pieces
-      // for bulk copies.
+      // stage a cluster partial, 4 whole fp32 rows per piece.
       auto piece = [&](int q) { return pbuf + (q >> 1) * LY::QB + (q & 1) * NPAD * 128 + hbase * 128; };
       // Workspace or cluster partial (unnormalised), or a whole result.  In
       // the stream form a unit cut by the CTA's range edge is a partial in
@@ -618,23 +614,12 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
           ms.inv_l[h] = unit_bad || den == 0.f ? 0.f : 1.f / den;
         }
         named_barrier(bar, kSoftmaxThreads);
-        {
+        // Output rows straight from registers: a warp writes 64 consecutive
+        // bytes of a row per store.
+        uint16_t* const dst = reinterpret_cast<uint16_t*>(a.out) + ((size_t)ui.s * H + h0 + hbase) * HD + row;
 #pragma unroll
-          for (int hl = 0; hl < HPG; ++hl) {
-            if (hl < my_heads) {
-              uint16_t* dst = reinterpret_cast<uint16_t*>(piece(hl >> 3)) + (hl & 7) * HD + row;
-              *dst = (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[hbase + hl], 0.f);
-            }
-          }
-          fence_proxy_async_smem();
-          named_barrier(bar, kSoftmaxThreads);
-          if (leader) {
-            for (int q = 0; q * 8 < my_heads; ++q)
-              bulk_store(static_cast<char*>(a.out) + ((size_t)ui.s * H + h0 + hbase + q * 8) * HD * 2,
-                         piece(q), (uint32_t)(min(8, my_heads - q * 8) * HD * 2));
-            bulk_commit();          // waited for before this warpgroup's next P rows
-          }
-        }
+        for (int hl = 0; hl < HPG; ++hl)
+          if (hl < my_heads) dst[hl * HD] = (uint16_t)pack2<BF16>(o_acc[hl] * ms.inv_l[hbase + hl], 0.f);
       }
 #pragma unroll
       for (int h = 0; h < HPG; ++h) o_acc[h] = l_part[h] = 0.f;
@@ -646,8 +631,6 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp >= 2 && warp < kVWarp && ((threadIdx.x - 64) & (kSoftmaxThreads - 1)) == 0)
-    bulk_wait_all();   // output stores complete before exit
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

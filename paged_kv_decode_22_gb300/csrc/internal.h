@@ -27,6 +27,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Arguments of one decode-attention launch, already validated on the host.
+// Stream form: a (sequence, KV head) pair whose last tile is partial counts
+// this many more positions in the tile list than it has tiles -- what ending
+// such a unit costs, in tile times (its last P V waits for a V tile that
+// lands late) -- so that CTAs whose share ends more of them take fewer tiles.
+constexpr int kStreamTailCost = 2;
+constexpr int kStreamTile = 128;   // tokens per tile of the stream form (its partition size)
+
 struct DecodeArgs {
   void* out;
   const void* q;
@@ -50,14 +57,16 @@ struct DecodeArgs {
   int fused;            // tensor-core path only: the partitions of one (sequence,
                         // KV head) form one thread-block cluster and are merged
                         // through distributed shared memory (no workspace)
-  int stream;           // tensor-core path only: CTA b takes tiles [T b / G, T (b + 1) / G)
-                        // of all (sequence, KV head) pairs in order (partition_size = 128,
-                        // num_partitions = 1); a unit cut by a range edge leaves a partial
-                        // in slot 2b (the CTA's first unit) or 2b + 1 (its last)
+  int stream;           // tensor-core path only: CTA b takes positions [T b / G, T (b + 1) / G)
+                        // of the list of all (sequence, KV head) pairs in order, each pair
+                        // its tiles then, when its last tile is partial, kStreamTailCost
+                        // empty positions (partition_size = 128, num_partitions = 1); a
+                        // unit cut by a range edge leaves a partial in slot 2b (the pair
+                        // began before the CTA's range) or 2b + 1 (it begins inside)
   int stream_ctas;      // stream: G, the grid size
   int4* ws_desc;        // stream: [G] the (sequence, KV head) cut by the left edge of CTA
-                        // b's range, written by CTA b: {first tile A, tiles n, s * Hk + hk,
-                        // total tiles T}; n = 0 when no pair is cut there
+                        // b's range, written by CTA b: {position A of its first tile, tiles n,
+                        // s * Hk + hk, total positions T}; n = 0 when no pair is cut there
   const int32_t* query_start;   // prefill: [S + 1] cumulative chunk lengths (nullptr: decode)
   int q_per_unit;       // prefill: query tokens per work unit
   int max_query_len;    // prefill: longer chunks are invalid (zero rows)

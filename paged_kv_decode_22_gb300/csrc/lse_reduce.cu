@@ -80,11 +80,12 @@ __global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(const DecodeArg
   for (int i = 0; i < E / 2; ++i) out[i] = pack2<BF16>(acc[2 * i] * inv, acc[2 * i + 1] * inv);
 }
 
-// Stream form: the tiles of (sequence s, KV head) are [A, A + n) of the
-// tile list, CTA b held [T b / G, T (b + 1) / G).  A pair cut by a range edge
-// left partials: CTA b0 (holding tile A) in slot 2 b0 when its range starts at
-// A (the pair was its first unit) or 2 b0 + 1 (its last), and every later CTA
-// up to b1 (holding tile A + n - 1) whose range is not empty in slot 2b.  One
+// Stream form: the tiles of (sequence s, KV head) sit at positions
+// [A, A + n) of the position list (each pair's tiles, then empty positions
+// when its last tile is partial), CTA b held [T b / G, T (b + 1) / G).  A pair
+// cut by a range edge left partials: CTA b0 (holding position A; the pair
+// begins inside its range) in slot 2 b0 + 1, and every later CTA up to b1
+// (holding A + n - 1) whose range is not empty in slot 2b.  One
 // column of blocks per range edge (16 heads per block, a warp per head); the
 // column of the pair's first cut (b0 + 1) merges it.
 constexpr int kMergeWarps = 16;
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) stream_merge_kernel(const De
   const int g = a.num_heads / a.num_kv_heads;
   const long long row0 = (long long)dsc.z * g;   // output row of head 0 of the pair
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int first_slot = 2 * b0 + ((T * b0) / G == A ? 0 : 1);
+  const int first_slot = 2 * b0 + 1;
   const int j = blockIdx.y * kMergeWarps + warp;
   if (j < g) {
     float acc[E] = {0.f, 0.f, 0.f, 0.f};

@@ -10,10 +10,12 @@
 // With more sequences CTAs take units round-robin and skip the empty ones.
 // In the cluster form of the tensor-core kernel each CTA takes the single
 // unit its grid position names (x = partition, y = sequence * Hk + KV head).
-// In the stream form the prefix counts 128-token tiles and CTA b takes the
-// tiles [T b / G, T (b + 1) / G) of the (sequence, KV head)-major tile list:
-// a unit is a run of them inside one (sequence, KV head), and only a CTA's
-// first and last units can be cut short (partials in slots 2b and 2b + 1).
+// In the stream form the prefix counts positions -- each (sequence, KV
+// head) pair's 128-token tiles, followed by kStreamTailCost empty positions
+// when its last tile is partial -- and CTA b takes the positions
+// [T b / G, T (b + 1) / G): a unit is the run of its tiles inside one pair,
+// and only a CTA's first and last units can be cut short (partials in slots
+// 2b and 2b + 1).
 // For prefill a unit is (sequence, KV head, query tile) and reads the cache
 // from token 0 up to the position of the tile's last query.
 #pragma once
@@ -40,6 +42,11 @@ struct UnitInfo {
   // position pos0, query c at pos0 + c.
   int qrow0, nq, pos0;
 };
+
+// Stream form: empty positions after each pair of a sequence of length L.
+__device__ __forceinline__ int stream_pad(int L) {
+  return L % kStreamTile ? kStreamTailCost : 0;
+}
 
 __device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
   return (len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && L > 0)
@@ -102,9 +109,9 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
 
 struct UnitCursor {
   long long next, end;
-  bool dense, first;
+  bool dense;
   int s, hk, p, np;   // dense: position of the last unit returned (np < 0: none yet);
-                      // stream: position of the next tile (np = tiles of sequence s)
+                      // stream: position of the next tile (np = positions per pair of s)
 };
 
 __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
@@ -114,7 +121,6 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
   c.dense = !a.fused && !a.query_start && a.num_seqs <= kSchedMax;
   c.s = c.hk = c.p = 0;
   c.np = -1;
-  c.first = true;
   if (a.stream) {
     // Stream form: an equal contiguous range of the sequence-major tile list.
     const long long total = sc.total;
@@ -140,44 +146,56 @@ template <int TT, bool PF = false>
 __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
                                             const DecodeArgs& a, UnitInfo& ui) {
   if (a.stream && !PF) {
-    // Units are the runs of the CTA's tile range inside one (sequence, KV
-    // head); pre[] counts tiles (partition_size = TT), so np = tiles of s.
-    if (c.next >= c.end) return false;
-    const int t = (int)c.next;
-    if (c.np < 0) {
-      int lo = 0, hi = a.num_seqs - 1;   // last s with pre[s] <= t
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sc.pre[mid] <= t) lo = mid; else hi = mid - 1;
+    // Units are the runs of the CTA's range over one pair's tiles; np =
+    // positions per pair of sequence s (its tiles and empty positions).
+    while (c.next < c.end) {
+      if (c.np < 0) {
+        const int t = (int)c.next;
+        int lo = 0, hi = a.num_seqs - 1;   // last s with pre[s] <= t
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (sc.pre[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        c.s = lo;
+        c.np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;
+        const int r = t - sc.pre[lo];
+        c.hk = r / c.np;
+        c.p = r - c.hk * c.np;
       }
-      c.s = lo;
-      c.np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;
-      const int r = t - sc.pre[lo];
-      c.hk = r / c.np;
-      c.p = r - c.hk * c.np;
-    }
-    const int off = c.p;
-    const int n = (int)min((long long)(c.np - off), c.end - c.next);
-    ui.s = c.s;
-    ui.hk = c.hk;
-    ui.p = 0;
-    ui.L = sc.L[c.s];
-    ui.lok = true;
-    ui.t0 = off * TT;
-    ui.t1 = min(ui.L, (off + n) * TT);
-    ui.ntiles = n;
-    ui.slot = (off > 0 || off + n < c.np) ? 2 * (int)blockIdx.x + (c.first ? 0 : 1) : -1;
-    c.first = false;
-    c.next += n;
-    if (c.next < c.end) {                // step to the next tile's (sequence, KV head)
-      c.p = 0;
-      if (++c.hk == a.num_kv_heads) {
-        c.hk = 0;
-        do { ++c.s; } while (sc.pre[c.s + 1] == sc.pre[c.s]);
-        c.np = (sc.pre[c.s + 1] - sc.pre[c.s]) / a.num_kv_heads;
+      const int nt = c.np - stream_pad(sc.L[c.s]);   // tiles of the pair
+      const int off = c.p;
+      if (off < nt) {
+        const int n = (int)min((long long)(nt - off), c.end - c.next);
+        ui.s = c.s;
+        ui.hk = c.hk;
+        ui.p = 0;
+        ui.L = sc.L[c.s];
+        ui.lok = true;
+        ui.t0 = off * TT;
+        ui.t1 = min(ui.L, (off + n) * TT);
+        ui.ntiles = n;
+        // A cut pair that began before the range is its first unit (slot
+        // 2b); one that begins inside runs past the range end (2b + 1).
+        ui.slot = (off > 0 || off + n < nt)
+                      ? 2 * (int)blockIdx.x +
+                            (c.next - off >= (long long)sc.total * blockIdx.x / gridDim.x)
+                      : -1;
+        c.next += n;
+        c.p += n;
+        return true;
+      }
+      // The pair's empty positions: step to the next pair.
+      c.next += c.np - off;
+      if (c.next < c.end) {
+        c.p = 0;
+        if (++c.hk == a.num_kv_heads) {
+          c.hk = 0;
+          do { ++c.s; } while (sc.pre[c.s + 1] == sc.pre[c.s]);
+          c.np = (sc.pre[c.s + 1] - sc.pre[c.s]) / a.num_kv_heads;
+        }
       }
     }
-    return true;
+    return false;
   }
   if (c.dense) {
     if (c.next >= c.end) return false;
@@ -240,7 +258,8 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
     for (int i = threadIdx.x; i < a.num_seqs; i += nthreads) {
       const int L = a.context_lens[i];
       sc.L[i] = L;
-      sc.pre[i + 1] = (a.query_start ? prefill_parts(a, i, L) : parts_of(a, L)) * a.num_kv_heads;
+      const int n = a.query_start ? prefill_parts(a, i, L) : parts_of(a, L);
+      sc.pre[i + 1] = (a.stream && n > 0 ? n + stream_pad(L) : n) * a.num_kv_heads;
     }
     __syncthreads();
     if (warp == 0) {
@@ -275,8 +294,10 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
             if (sc.pre[mid] <= t) lo = mid; else hi = mid - 1;
           }
           const int np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;
-          const int r = t - sc.pre[lo], hk = r / np;
-          if (r - hk * np > 0) d = make_int4(sc.pre[lo] + hk * np, np, lo * a.num_kv_heads + hk, (int)T);
+          const int r = t - sc.pre[lo], hk = r / np, off = r - hk * np;
+          const int nt = np - stream_pad(sc.L[lo]);
+          if (off > 0 && off < nt)   // inside the pair's tiles
+            d = make_int4(sc.pre[lo] + hk * np, nt, lo * a.num_kv_heads + hk, (int)T);
         }
         a.ws_desc[blockIdx.x] = d;
       }
