@@ -39,7 +39,10 @@ METRIC = ("paged decode attn µs/call and achieved HBM GB/s (% of GB300 roofline
 WORKLOAD = "llama13b_mha_b8_ctx256 decode + gather_t2048"
 DECODE_CFG = "llama13b_mha_b8_ctx256"
 GATHER_CFG = "gather_t2048"
-TARGETS = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "gqa_ctx4096_b256"]
+# Decode workloads at batch >= 64 and context >= 1024, reported beside the
+# default line (decode alone).
+TARGETS = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "gqa_ctx4096_b256",
+           "mqa_ragged_b64"]
 PATH_NAMES = {0: "simt", 1: "tc", 2: "tc_cluster", 3: "tc_stream"}   # decode_plan's kernel family
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
@@ -673,7 +676,7 @@ def main():
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
 
-    # Large-batch GQA lines (decode alone): inputs from a seeded torch
+    # Large-batch decode lines (decode alone): inputs from a seeded torch
     # generator on the device (timing does not depend on the values), CUDA
     # graph replays over rotated copies, as in the timed region above.
     targets = {}
@@ -741,7 +744,7 @@ def main():
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
-        "targets_decode_bf16_gqa64x8": targets,
+        "targets_decode": targets,
         "targets_prefill": prefill_lines,
     }
     if world == 1 and not args.no_cpu:

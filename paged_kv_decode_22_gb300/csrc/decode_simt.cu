@@ -15,10 +15,11 @@
 // memory) and the query are requested together at entry, so only one global
 // round trip precedes the first K/V load.  Table entries of the partition past
 // the sequence end are read with the others but never used.  K and V reach
-// shared memory by TMA: each warp owns a ring of 4 stages, one stage being
+// shared memory by TMA: each warp owns a ring of 2 stages, one stage being
 // the K and V rows of 8 consecutive tokens of one block (two boxes, 4 KB at
-// head_size 128), so a warp keeps up to 16 KB of loads in flight while it
-// computes, with two TMA instructions per 8 tokens.  Rows a box brings in
+// head_size 128), so a warp keeps up to 8 KB of loads in flight while it
+// computes, with two TMA instructions per 8 tokens.  The small ring (32 KB
+// per CTA) lets many CTAs share an SM, the next call's among them.  Rows a box brings in
 // past the partition end or the sequence end are masked (their V is read as
 // zero: cache slots past the end may hold anything, NaN included); boxes of
 // out-of-range block ids read an out-of-bounds row, which TMA fills with zeros.
@@ -55,7 +56,7 @@ using namespace sm100;
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRows = 8;        // tokens per warp iteration = rows of one TMA box
-constexpr int kStages = 4;      // ring depth per warp
+constexpr int kStages = 2;      // ring depth per warp
 constexpr int kMaxIds = 1024;   // block ids staged in shared memory per pass
 
 template <int D>

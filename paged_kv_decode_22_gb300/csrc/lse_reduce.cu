@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(const DecodeArg
 // (holding A + n - 1) whose range is not empty in slot 2b.  One
 // column of blocks per range edge (16 heads per block, a warp per head); the
 // column of the pair's first cut (b0 + 1) merges it.
-constexpr int kMergeWarps = 16;
+constexpr int kMergeWarps = 8;
 constexpr int kMergeChunk = 8;    // partial slots loaded at once
 
 __device__ __forceinline__ int cta_of(long long t, long long T, int G) {   // holder of tile t
