@@ -322,7 +322,7 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
     return;
   }
   for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
-    const int L = a.context_lens[sq];
+    const int L = a.num_seqs <= kSchedMax ? sc.L[sq] : a.context_lens[sq];
     if (parts_of(a, L) == 0) {
       if (!len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) && threadIdx.x == 0)
         flag(a.status, PKD_DEV_BAD_LEN);
