@@ -30,7 +30,8 @@ constexpr int kSchedMax = 1024;
 struct SchedSmem {
   int total;
   int L[kSchedMax];        // context length of each sequence
-  int pre[kSchedMax + 1];  // units of the sequences before s
+  int pre[kSchedMax + 1];  // units (stream: positions) of the sequences before s;
+                           // prefill: query_start
 };
 
 struct UnitInfo {
@@ -56,15 +57,14 @@ __device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
 
 // Prefill: a sequence's units are its query tiles of q_per_unit queries; a
 // chunk longer than the context or than max_query_len (or an invalid
-// length) has none.
-__device__ __forceinline__ bool chunk_rows_ok(const DecodeArgs& a, int s) {
-  const int q0 = a.query_start[s], q1 = a.query_start[s + 1];
+// length) has none.  q0, q1 = query_start[s], query_start[s + 1].
+__device__ __forceinline__ bool chunk_rows_ok(const DecodeArgs& a, int q0, int q1) {
   return 0 <= q0 && q0 <= q1 && q1 <= a.num_q_tokens;   // rows inside q / out
 }
 
-__device__ __forceinline__ int prefill_parts(const DecodeArgs& a, int s, int L) {
-  const int n = a.query_start[s + 1] - a.query_start[s];
-  return (chunk_rows_ok(a, s) && len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) &&
+__device__ __forceinline__ int prefill_parts(const DecodeArgs& a, int q0, int q1, int L) {
+  const int n = q1 - q0;
+  return (chunk_rows_ok(a, q0, q1) && len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) &&
           n > 0 && n <= L && n <= a.max_query_len)
              ? (n + a.q_per_unit - 1) / a.q_per_unit
              : 0;
@@ -73,9 +73,8 @@ __device__ __forceinline__ int prefill_parts(const DecodeArgs& a, int s, int L) 
 // Token range and queries of prefill unit (s, query tile p): the unit reads
 // the cache up to its last query's position.
 template <int TT>
-__device__ __forceinline__ void prefill_unit(const DecodeArgs& a, UnitInfo& ui) {
-  const int q0 = a.query_start[ui.s];
-  const int n = a.query_start[ui.s + 1] - q0;
+__device__ __forceinline__ void prefill_unit(const DecodeArgs& a, int q0, int q1, UnitInfo& ui) {
+  const int n = q1 - q0;
   const int i0 = ui.p * a.q_per_unit;
   ui.nq = min(a.q_per_unit, n - i0);
   ui.qrow0 = q0 + i0;
@@ -85,8 +84,10 @@ __device__ __forceinline__ void prefill_unit(const DecodeArgs& a, UnitInfo& ui) 
   ui.ntiles = (ui.t1 + TT - 1) / TT;
 }
 
+// With at most kSchedMax sequences prefill reads lengths and chunk bounds
+// from the shared-memory schedule (sc.L, and sc.pre holding query_start).
 template <int TT, bool PF>
-__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
+__device__ __forceinline__ UnitInfo unit_info(const SchedSmem& sc, const DecodeArgs& a, int u) {
   UnitInfo ui;
   const int P = a.num_partitions;
   // Prefill: a sequence's later query tiles see more of the cache, so they
@@ -95,12 +96,17 @@ __device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
   const int sh = u / P;
   ui.hk = sh % a.num_kv_heads;
   ui.s = sh / a.num_kv_heads;
-  ui.L = a.context_lens[ui.s];
-  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
   if constexpr (PF) {
-    if (ui.p < prefill_parts(a, ui.s, ui.L)) prefill_unit<TT>(a, ui); else ui.ntiles = 0;
+    const bool smem = a.num_seqs <= kSchedMax;
+    ui.L = smem ? sc.L[ui.s] : a.context_lens[ui.s];
+    ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
+    const int q0 = smem ? sc.pre[ui.s] : a.query_start[ui.s];
+    const int q1 = smem ? sc.pre[ui.s + 1] : a.query_start[ui.s + 1];
+    if (ui.p < prefill_parts(a, q0, q1, ui.L)) prefill_unit<TT>(a, q0, q1, ui); else ui.ntiles = 0;
     return ui;
   }
+  ui.L = a.context_lens[ui.s];
+  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
   ui.t0 = ui.p * a.partition_size;
   ui.t1 = min(ui.t0 + a.partition_size, ui.L);
   ui.ntiles = (ui.lok && ui.t0 < ui.L) ? (ui.t1 - ui.t0 + TT - 1) / TT : 0;
@@ -227,17 +233,13 @@ __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
     ui.hk = c.hk;
     ui.p = c.p;
     ui.lok = true;
-    if constexpr (PF) {
-      prefill_unit<TT>(a, ui);
-      return true;
-    }
     ui.t0 = ui.p * a.partition_size;
     ui.t1 = min(ui.t0 + a.partition_size, ui.L);
     ui.ntiles = (ui.t1 - ui.t0 + TT - 1) / TT;
     return true;
   }
   while (c.next < c.end) {
-    ui = unit_info<TT, PF>(a, (int)c.next);
+    ui = unit_info<TT, PF>(sc, a, (int)c.next);
     c.next += gridDim.x;
     if (ui.ntiles) return true;
   }
@@ -254,11 +256,18 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
     __syncthreads();
     return;
   }
-  if (a.num_seqs <= kSchedMax) {
+  if (a.num_seqs <= kSchedMax && a.query_start) {
+    // Prefill takes units round-robin: the table keeps lengths and chunk
+    // bounds (pre = query_start) for the cursor.
+    for (int i = threadIdx.x; i <= a.num_seqs; i += nthreads) {
+      if (i < a.num_seqs) sc.L[i] = a.context_lens[i];
+      sc.pre[i] = a.query_start[i];
+    }
+  } else if (a.num_seqs <= kSchedMax) {
     for (int i = threadIdx.x; i < a.num_seqs; i += nthreads) {
       const int L = a.context_lens[i];
       sc.L[i] = L;
-      const int n = a.query_start ? prefill_parts(a, i, L) : parts_of(a, L);
+      const int n = parts_of(a, L);
       sc.pre[i + 1] = (a.stream && n > 0 ? n + stream_pad(L) : n) * a.num_kv_heads;
     }
     __syncthreads();
@@ -308,10 +317,10 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
     // invalid length, or longer than the context) and flag them.
     for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
       const int L = a.context_lens[sq];
-      const int q0 = a.query_start[sq], n = a.query_start[sq + 1] - q0;
-      if (!chunk_rows_ok(a, sq)) {         // rows outside q / out: nothing can be written
+      const int q0 = a.query_start[sq], q1 = a.query_start[sq + 1], n = q1 - q0;
+      if (!chunk_rows_ok(a, q0, q1)) {     // rows outside q / out: nothing can be written
         if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
-      } else if (n > 0 && prefill_parts(a, sq, L) == 0) {
+      } else if (n > 0 && prefill_parts(a, q0, q1, L) == 0) {
         if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
         uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)q0 * a.num_heads * a.head_size / 2;
         const size_t words = (size_t)n * a.num_heads * a.head_size / 2;

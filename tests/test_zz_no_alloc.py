@@ -44,9 +44,13 @@ def _case(seed, lens, H, Hk, dtype):
                                        num_blocks=need + 5, context_lens=lens, dtype=dtype))
 
 
-@pytest.mark.parametrize("partition_size", [128, 0])
+@pytest.mark.parametrize("partition_size", [128, 0, -1])
 def test_static_scratch_entry_matches_ordinary_entry_twice(partition_size):
-    cases = [_case(31, [4096, 777], 64, 8, "bf16"), _case(32, [3000, 129, 2048], 16, 16, "fp16")]
+    # -1: the stream form (tensor-core shapes only); its scratch holds two
+    # partial slots per SM and the range-edge descriptors.
+    cases = [_case(31, [4096, 777], 64, 8, "bf16"),
+             _case(32, [3000, 129, 2048], 16, 16, "fp16") if partition_size >= 0
+             else _case(34, [5000, 1, 0, 3333], 48, 1, "fp16")]
     for dc in cases:                         # two calls in a row, different inputs
         c = dc.c
         _, npart, _, ws_bytes = ops.decode_plan(c.num_seqs, c.num_heads, c.num_kv_heads, 128,
