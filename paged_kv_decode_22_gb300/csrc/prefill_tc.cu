@@ -292,8 +292,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int H = a.num_heads;
     const int qi = row / g, hj = row - qi * g; // row = (chunk query qi, head hj of the group)
     const bool alibi = a.alibi != nullptr;
-    uint32_t j = 0, u = 0;
+    uint32_t j = 0, u = 0, u_fin = 0;   // u_fin: units whose output is written
     bool ok = true;
+    // A unit's output is written after the next unit's first P, so its last
+    // P V runs while that tile's softmax does: the pending write's state.
+    bool pend = false, pend_valid = false;
+    int pend_ub = 0;
+    float pend_inv = 0.f;
+    uint4* pend_dst = nullptr;
+    auto finalize = [&]() {
+      ok = ok && mbar_wait(&ms.o_full[pend_ub], (u_fin >> 1) & 1);
+      if (!ok) return;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld32(lane_addr + 256 + pend_ub * 128 + c * 32, v);
+        if (pend_valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            pend_dst[c * 4 + i] = make_uint4(pack2<BF16>(v[8 * i] * pend_inv, v[8 * i + 1] * pend_inv),
+                                             pack2<BF16>(v[8 * i + 2] * pend_inv, v[8 * i + 3] * pend_inv),
+                                             pack2<BF16>(v[8 * i + 4] * pend_inv, v[8 * i + 5] * pend_inv),
+                                             pack2<BF16>(v[8 * i + 6] * pend_inv, v[8 * i + 7] * pend_inv));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&ms.o_empty[pend_ub]);
+      pend = false;
+      ++u_fin;
+    };
     UnitCursor cur = cursor_begin(ms.sched, a);
     UnitInfo ui;
     while (ok && cursor_next<TT, true>(cur, ms.sched, a, ui)) {
@@ -409,33 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ms.p_full[b]);
+        if (pend) finalize();   // the previous unit's output, its last P V now done
       }
       if (!ok) break;
       // ---------------------------------------------------------- finalise unit
-      ok = mbar_wait(&ms.o_full[ub], (u >> 1) & 1);
-      if (!ok) break;
-      tc_fence_after();
-      const bool zero = !valid_row || pos >= bad_from || l == 0.f;
-      const float inv = zero ? 0.f : 1.f / l;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                            ((size_t)(ui.qrow0 + qi) * H + ui.hk * g + hj) * HD);
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        float v[32];
-        tmem_ld32(lane_addr + 256 + ub * 128 + c * 32, v);
-        if (valid_row) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[c * 4 + i] = make_uint4(pack2<BF16>(v[8 * i] * inv, v[8 * i + 1] * inv),
-                                        pack2<BF16>(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
-                                        pack2<BF16>(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
-                                        pack2<BF16>(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&ms.o_empty[ub]);
+      // (written after the next unit's first P, or after the last unit)
+      pend = true;
+      pend_ub = ub;
+      pend_valid = valid_row;
+      pend_inv = !valid_row || pos >= bad_from || l == 0.f ? 0.f : 1.f / l;
+      pend_dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                          ((size_t)(ui.qrow0 + qi) * H + ui.hk * g + hj) * HD);
       ++u;
     }
+    if (ok && pend) finalize();
     if (!ok && threadIdx.x == 128) set_abort(ms, a.status);
   }
 
