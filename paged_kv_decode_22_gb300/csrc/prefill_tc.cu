@@ -27,6 +27,12 @@
 //              columns of the tile's S buffer, the A operand of P V.
 // TMEM: S double-buffered (2 x 128 columns), O double-buffered by unit
 // parity (2 x 128), 512 columns.
+//
+// Paired form (chunks of several query tiles, g >= 2): a cluster of two CTAs
+// takes two query tiles of one (sequence, KV head) in lockstep; each K tile
+// is loaded once by rank 0 and each V tile once by rank 1, TMA-multicast into
+// both CTAs, so each SM issues half the boxes.  Stage release counts both
+// CTAs' MMA commits (multicast tcgen05.commit).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -72,7 +78,57 @@ __device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
   flag(status, PKD_DEV_TIMEOUT);
 }
 
-template <bool BF16>
+// Units of one CTA.  Single form: the shared schedule, dealt round-robin.
+// Paired form (PAIR): the two CTAs of a cluster take the query tiles 2pp and
+// 2pp + 1 of one (sequence, KV head) together -- pairs dealt round-robin over
+// the clusters, later (heavier) pairs first -- and both walk the pair's
+// tiles (the longer unit's count), so that every K/V tile is loaded once for
+// both.  A CTA whose own tile is absent runs a unit without valid rows, and
+// the shorter unit's extra tiles lie past all of its queries (fully masked).
+template <bool PAIR>
+struct PfCursor {
+  UnitCursor uc;
+  long long next, end;
+  int stride;
+  __device__ __forceinline__ void begin(const SchedSmem& sc, const DecodeArgs& a) {
+    if constexpr (PAIR) {
+      next = blockIdx.x >> 1;
+      stride = gridDim.x >> 1;
+      end = (long long)a.num_seqs * a.num_kv_heads * ((a.num_partitions + 1) / 2);
+    } else {
+      uc = cursor_begin(sc, a);
+    }
+  }
+  __device__ __forceinline__ bool step(const SchedSmem& sc, const DecodeArgs& a, UnitInfo& ui) {
+    if constexpr (PAIR) {
+      const int PP = (a.num_partitions + 1) / 2;
+      while (next < end) {
+        const int v = (int)next;
+        next += stride;
+        const int pp = PP - 1 - v % PP, sh = v / PP;
+        const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
+        const UnitInfo u0 = prefill_unit_at<TT>(sc, a, s, hk, 2 * pp);
+        const UnitInfo u1 = prefill_unit_at<TT>(sc, a, s, hk, 2 * pp + 1);
+        if (u0.ntiles == 0 && u1.ntiles == 0) continue;
+        ui = cluster_ctarank() ? u1 : u0;
+        if (ui.ntiles == 0) {   // no valid rows; q rows read from row 0 (unused)
+          ui.nq = 0;
+          ui.qrow0 = 0;
+          ui.pos0 = 0;
+          ui.t0 = 0;
+        }
+        ui.t1 = max(u0.ntiles ? u0.t1 : 0, u1.ntiles ? u1.t1 : 0);
+        ui.ntiles = max(u0.ntiles, u1.ntiles);
+        return true;
+      }
+      return false;
+    } else {
+      return cursor_next<TT, true>(uc, sc, a, ui);
+    }
+  }
+};
+
+template <bool BF16, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
@@ -87,17 +143,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = a.num_heads / a.num_kv_heads;
+  // Paired form: rank 0 loads K into both CTAs of the cluster, rank 1 V; a
+  // stage is free once the MMAs of both CTAs are done with it (and, for K,
+  // this CTA's softmax has read the stage's bad-block entry: without that
+  // arrival a stage could be refilled twice before the softmax checks it).
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  constexpr uint32_t kMmaCount = PAIR ? 2 : 1;
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) {
       mbar_init(&ms.k_full[i], 1);
-      mbar_init(&ms.k_empty[i], 1 + kSoftmaxThreads);
+      mbar_init(&ms.k_empty[i], kMmaCount + kSoftmaxThreads);
       ms.k_bad[i] = -1;
     }
     for (int i = 0; i < NV; ++i) {
       mbar_init(&ms.v_full[i], 1);
-      mbar_init(&ms.v_empty[i], 1);
+      mbar_init(&ms.v_empty[i], kMmaCount);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms.q_full[i], 1);
@@ -119,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ms.tmem_base, 512);
     tmem_relinquish();
   }
+  if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any multicast
   pdl_wait();
   pdl_launch_dependents();
   schedule_setup(ms.sched, a, kThreads);
@@ -134,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1 both halves of V.
     const bool is_v = warp == 1;
     const bool primary = warp != 3;
+    const bool issues = !PAIR || rank == (is_v ? 1u : 0u);   // this CTA loads the operand
     const int half_mask = warp == 0 ? 1 : warp == 3 ? 2 : 3;
     const int B = a.block_size;
     const int R = B < TT ? B : TT;            // rows per TMA box
@@ -155,9 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return raw;
     };
-    UnitCursor cur = cursor_begin(ms.sched, a);
+    PfCursor<PAIR> cur;
+    cur.begin(ms.sched, a);
     UnitInfo ui;
-    bool have = cursor_next<TT, true>(cur, ms.sched, a, ui);
+    // (K's second-half warp of the CTA that does not load K has nothing to do.)
+    bool have = (issues || primary) && cur.step(ms.sched, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -167,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool nhave = true;
       int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nhave = cursor_next<TT, true>(cur, ms.sched, a, nui);
+        nhave = cur.step(ms.sched, a, nui);
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
@@ -200,9 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const int r = __shfl_sync(0xffffffffu, row, my_box);
-      if (issuer)
-        tma_load_3d(ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128, map,
-                    &full[st], my_half * 64, ui.hk, r);
+      if (issuer && issues) {
+        uint8_t* dst = ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128;
+        if constexpr (PAIR)
+          tma_load_3d_mc(dst, map, &full[st], my_half * 64, ui.hk, r, 3);
+        else
+          tma_load_3d(dst, map, &full[st], my_half * 64, ui.hk, r);
+      }
       ++jk;
       if (njl == 0) ++un;
       have = nhave;
@@ -243,13 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         kSwizzle128B);
           mma_f16_ts(d, tmem + b * 128 + k * 8, bd, id_o, !(pv_first && k == 0));
         }
-        mma_commit(&ms.v_empty[vs]);
+        if constexpr (PAIR) mma_commit_mc(&ms.v_empty[vs], 3); else mma_commit(&ms.v_empty[vs]);
         mma_commit(&ms.pv_done[b]);
         if (pv_last) mma_commit(&ms.o_full[ub]);
       };
-      UnitCursor cur = cursor_begin(ms.sched, a);
+      PfCursor<PAIR> cur;
+      cur.begin(ms.sched, a);
       UnitInfo ui;
-      while (ok && cursor_next<TT, true>(cur, ms.sched, a, ui)) {
+      while (ok && cur.step(ms.sched, a, ui)) {
         const int qb = un & 1;
         ok = ok && mbar_wait(&ms.q_full[qb], (un >> 1) & 1);
         for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++j) {
@@ -267,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(d, ad, bd, id_s, k > 0);
           }
           mma_commit(&ms.s_full[b]);
-          mma_commit(&ms.k_empty[ks]);
+          if constexpr (PAIR) mma_commit_mc(&ms.k_empty[ks], 3); else mma_commit(&ms.k_empty[ks]);
           if (jl == ui.ntiles - 1) mma_commit(&ms.q_empty[qb]);
           if (pv_j >= 0) issue_pv();
           pv_j = (int)j;
@@ -322,9 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       pend = false;
       ++u_fin;
     };
-    UnitCursor cur = cursor_begin(ms.sched, a);
+    PfCursor<PAIR> cur;
+    cur.begin(ms.sched, a);
     UnitInfo ui;
-    while (ok && cursor_next<TT, true>(cur, ms.sched, a, ui)) {
+    while (ok && cur.step(ms.sched, a, ui)) {
       const int ub = u & 1;
       const bool valid_row = qi < ui.nq;
       const int pos = valid_row ? ui.pos0 + qi : -1;      // last visible token
@@ -461,6 +533,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // Paired form: no CTA leaves while its partner may still load into it.
+  if constexpr (PAIR) cluster_sync();
+}
+
+// Maximum dynamic shared memory, set once per device and kernel.
+template <bool BF16, bool PAIR>
+cudaError_t prepare() {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(prefill_tc_kernel<BF16, PAIR>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+void pair_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&attr)[2], int grid,
+                 cudaStream_t st) {
+  *cfg = {};
+  cfg->gridDim = dim3(grid);
+  cfg->blockDim = dim3(kThreads);
+  cfg->dynamicSmemBytes = kSmemBytes;
+  cfg->stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 2;
+}
+
+// Co-resident two-CTA clusters of the paired kernel, cached per device (0:
+// none, the single form is used).
+template <bool BF16>
+int pair_capacity() {
+  static int cache[64];   // value + 1; 0 = not yet queried
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (prepare<BF16, true>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr[2];
+      pair_config(&cfg, attr, 2, nullptr);
+      if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<BF16, true>, &cfg) != cudaSuccess) {
+        cudaGetLastError();   // a refused query only means "no paired launch"
+        n = 0;
+      }
+    }
+    cache[dev] = n + 1;
+  }
+  return cache[dev] - 1;
 }
 
 template <bool BF16>
@@ -473,20 +603,28 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
       !make_kv_map(&vm, a.value_cache, BF16, HD, a.num_kv_heads, rows, 64, box_rows, true) ||
       !make_q_chunk_map(&qm, a.q, BF16, HD, a.num_heads, a.num_q_tokens, g, a.q_per_unit))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<BF16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Paired form where chunks span several query tiles of at most 64 queries
+  // (g >= 2): the two tiles of a pair then need the same K/V tiles.
+  if (a.num_partitions >= 2 && g >= 2) {
+    const int cap = pair_capacity<BF16>();
+    const long long pairs = (long long)a.num_seqs * a.num_kv_heads * ((a.num_partitions + 1) / 2);
+    if (cap > 0) {
+      const int clusters = (int)(pairs < cap ? pairs : cap);
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr[2];
+      pair_config(&cfg, attr, 2 * clusters, st);
+      return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<BF16, true>, km, vm, qm, a);
+    }
+  }
+  cudaError_t e = prepare<BF16, false>();
+  if (e != cudaSuccess) return e;
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   const int grid = (int)(units < sms ? units : sms);
-  return launch_pdl(prefill_tc_kernel<BF16>, dim3(grid), dim3(kThreads), kSmemBytes, st, km, vm,
-                    qm, a);
+  return launch_pdl(prefill_tc_kernel<BF16, false>, dim3(grid), dim3(kThreads), kSmemBytes, st,
+                    km, vm, qm, a);
 }
 
 }  // namespace

@@ -84,8 +84,27 @@ __device__ __forceinline__ void prefill_unit(const DecodeArgs& a, int q0, int q1
   ui.ntiles = (ui.t1 + TT - 1) / TT;
 }
 
-// With at most kSchedMax sequences prefill reads lengths and chunk bounds
-// from the shared-memory schedule (sc.L, and sc.pre holding query_start).
+// Prefill unit (sequence s, KV head hk, query tile p); ntiles = 0 when the
+// chunk has no such tile.  With at most kSchedMax sequences lengths and chunk
+// bounds come from the shared-memory schedule (sc.L, and sc.pre holding
+// query_start).
+template <int TT>
+__device__ __forceinline__ UnitInfo prefill_unit_at(const SchedSmem& sc, const DecodeArgs& a, int s,
+                                                    int hk, int p) {
+  UnitInfo ui;
+  ui.s = s;
+  ui.hk = hk;
+  ui.p = p;
+  ui.slot = -1;
+  const bool smem = a.num_seqs <= kSchedMax;
+  ui.L = smem ? sc.L[s] : a.context_lens[s];
+  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
+  const int q0 = smem ? sc.pre[s] : a.query_start[s];
+  const int q1 = smem ? sc.pre[s + 1] : a.query_start[s + 1];
+  if (p < prefill_parts(a, q0, q1, ui.L)) prefill_unit<TT>(a, q0, q1, ui); else ui.ntiles = 0;
+  return ui;
+}
+
 template <int TT, bool PF>
 __device__ __forceinline__ UnitInfo unit_info(const SchedSmem& sc, const DecodeArgs& a, int u) {
   UnitInfo ui;
@@ -96,15 +115,7 @@ __device__ __forceinline__ UnitInfo unit_info(const SchedSmem& sc, const DecodeA
   const int sh = u / P;
   ui.hk = sh % a.num_kv_heads;
   ui.s = sh / a.num_kv_heads;
-  if constexpr (PF) {
-    const bool smem = a.num_seqs <= kSchedMax;
-    ui.L = smem ? sc.L[ui.s] : a.context_lens[ui.s];
-    ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
-    const int q0 = smem ? sc.pre[ui.s] : a.query_start[ui.s];
-    const int q1 = smem ? sc.pre[ui.s + 1] : a.query_start[ui.s + 1];
-    if (ui.p < prefill_parts(a, q0, q1, ui.L)) prefill_unit<TT>(a, q0, q1, ui); else ui.ntiles = 0;
-    return ui;
-  }
+  if constexpr (PF) return prefill_unit_at<TT>(sc, a, ui.s, ui.hk, ui.p);
   ui.L = a.context_lens[ui.s];
   ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
   ui.t0 = ui.p * a.partition_size;
