@@ -29,10 +29,10 @@
 // parity (2 x 128), 512 columns.
 //
 // Paired form (chunks of several query tiles, g >= 2): a cluster of two CTAs
-// takes two query tiles of one (sequence, KV head) in lockstep; each K tile
-// is loaded once by rank 0 and each V tile once by rank 1, TMA-multicast into
-// both CTAs, so each SM issues half the boxes.  Stage release counts both
-// CTAs' MMA commits (multicast tcgen05.commit).
+// takes two query tiles of one (sequence, KV head) in lockstep; rank r loads
+// the 64-column half r of each K and V tile, TMA-multicast into both CTAs, so
+// each SM issues half the boxes and a tile's boxes leave two SMs at once.
+// Stage release counts both CTAs' MMA commits (multicast tcgen05.commit).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -143,8 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = a.num_heads / a.num_kv_heads;
-  // Paired form: rank 0 loads K into both CTAs of the cluster, rank 1 V; a
-  // stage is free once the MMAs of both CTAs are done with it (and, for K,
+  // Paired form: each CTA loads half of every K and V tile into both CTAs of
+  // the cluster; a stage is free once the MMAs of both CTAs are done with it (and, for K,
   // this CTA's softmax has read the stage's bad-block entry: without that
   // arrival a stage could be refilled twice before the softmax checks it).
   const uint32_t rank = PAIR ? cluster_ctarank() : 0;
@@ -197,8 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1 both halves of V.
     const bool is_v = warp == 1;
     const bool primary = warp != 3;
-    const bool issues = !PAIR || rank == (is_v ? 1u : 0u);   // this CTA loads the operand
-    const int half_mask = warp == 0 ? 1 : warp == 3 ? 2 : 3;
+    // Paired form: each CTA loads its own 64-column half (rank) of every K
+    // and V tile into both CTAs, so a tile's boxes leave two SMs at once.
+    const int half_mask = (warp == 0 ? 1 : warp == 3 ? 2 : 3) & (PAIR ? 1 << rank : 3);
     const int B = a.block_size;
     const int R = B < TT ? B : TT;            // rows per TMA box
     const int nbox = TT / R;                  // boxes per tile and 64-column half
@@ -222,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     PfCursor<PAIR> cur;
     cur.begin(ms.sched, a);
     UnitInfo ui;
-    // (K's second-half warp of the CTA that does not load K has nothing to do.)
-    bool have = (issues || primary) && cur.step(ms.sched, a, ui);
+    // (A warp with no half to load and no barrier to arm has nothing to do.)
+    bool have = (half_mask != 0 || primary) && cur.step(ms.sched, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const int r = __shfl_sync(0xffffffffu, row, my_box);
-      if (issuer && issues) {
+      if (issuer) {
         uint8_t* dst = ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128;
         if constexpr (PAIR)
           tma_load_3d_mc(dst, map, &full[st], my_half * 64, ui.hk, r, 3);
