@@ -29,6 +29,21 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_header_constants_match_the_binding():
+    """Every #define of include/pkd.h that the binding mirrors has the same value."""
+    import re
+    text = open(_lib.HEADER).read()
+    defs = {m.group(1): int(m.group(2)) for m in
+            re.finditer(r"#define\s+PKD_(\w+)\s+\(?(-?\d+)u?\)?", text)}
+    mirrored = {"PATH_SIMT": _lib.PATH_SIMT, "PATH_TC": _lib.PATH_TC,
+                "PATH_TC_CLUSTER": _lib.PATH_TC_CLUSTER, "PATH_TC_STREAM": _lib.PATH_TC_STREAM,
+                "PARTITION_STREAM": _lib.PARTITION_STREAM, "DEV_BAD_BLOCK": _lib.DEV_BAD_BLOCK,
+                "DEV_BAD_SLOT": _lib.DEV_BAD_SLOT, "DEV_BAD_LEN": _lib.DEV_BAD_LEN,
+                "DEV_TIMEOUT": _lib.DEV_TIMEOUT}
+    for name, value in mirrored.items():
+        assert defs.get(name) == value, (name, defs.get(name), value)
+
+
 def test_version_and_status_strings(lib):
     assert lib.pkd_version() >= 100
     for code in range(8):
@@ -53,7 +68,7 @@ def _decode(lib, **kw):
     (dict(dtype=5), 3), (dict(B=12), 3), (dict(B=4), 3), (dict(B=512), 3),
     (dict(NB=0), 2), (dict(mb=0), 2), (dict(q=MISALIGNED), 5), (dict(kc=MISALIGNED), 5),
     (dict(H=6, Hk=4), 2), (dict(S=0), 2), (dict(S=70000), 2), (dict(maxctx=-1), 2),
-    (dict(D=96), 3), (dict(NB=1 << 28, B=16), 2),
+    (dict(D=96), 3), (dict(NB=1 << 28, B=16), 2), (dict(ps=-2), 2),
 ])
 def test_decode_rejects_bad_arguments_on_host(lib, kw, code):
     assert _decode(lib, **kw) == code
