@@ -8,7 +8,7 @@
 // Work unit = (sequence, KV head, tile of QT = 128 / g chunk queries): its
 // 128 rows are the (query, head) pairs r = query * g + head, so all g heads
 // of a query share every K/V tile.  A persistent grid of one CTA per SM walks
-// the units (the shared schedule of the decode kernel); inside the CTA:
+// the units, dealt round-robin; inside the CTA:
 //   warps 0, 3 K producers (half 0 and the unit's Q tile; half 1): TMA boxes of one block x
 //              64 columns into a ring of 32 KB stages, block ids one tile
 //              ahead, out-of-range blocks from an out-of-bounds row (zeros).
@@ -51,6 +51,7 @@ constexpr int ROWS = 128;                // (query, head) rows per unit (= MMA M
 constexpr int TILE_BYTES = TT * HD * 2;  // one K or V tile, 32 KB
 constexpr int Q_BYTES = ROWS * HD * 2;   // one Q tile, 32 KB
 constexpr int NK = 2, NV = 2;            // ring stages
+constexpr int kPfTable = 128;            // sequences whose lengths and chunk bounds sit in shared memory
 constexpr int kThreads = 256;            // 8 warps
 constexpr int kSoftmaxThreads = 128;
 constexpr int kNoBlock = -2147483647 - 1;
@@ -67,48 +68,117 @@ struct Misc {
   uint32_t tmem_base;
   int abort;
   int k_bad[NK];      // per K stage: token offset of the tile's first bad block id, or -1
-  SchedSmem sched;
+  int tab_L[kPfTable];        // context_lens, with at most kPfTable sequences
+  int tab_qs[kPfTable + 1];   // query_start, likewise
 };
-constexpr int kMiscBytes = 8704;
+constexpr int kMiscBytes = 1280;
 static_assert(sizeof(Misc) <= kMiscBytes, "misc area too small");
 constexpr int kSmemBytes = off_misc + kMiscBytes + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "above the shared memory of one CTA");
 
 __device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
   ms.abort = 1;
   flag(status, PKD_DEV_TIMEOUT);
 }
 
-// Units of one CTA.  Single form: the shared schedule, dealt round-robin.
-// Paired form (PAIR): the two CTAs of a cluster take the query tiles 2pp and
-// 2pp + 1 of one (sequence, KV head) together -- pairs dealt round-robin over
-// the clusters, later (heavier) pairs first -- and both walk the pair's
-// tiles (the longer unit's count), so that every K/V tile is loaded once for
-// both.  A CTA whose own tile is absent runs a unit without valid rows, and
-// the shorter unit's extra tiles lie past all of its queries (fully masked).
-template <bool PAIR>
-struct PfCursor {
-  UnitCursor uc;
-  long long next, end;
-  int stride;
-  __device__ __forceinline__ void begin(const SchedSmem& sc, const DecodeArgs& a) {
-    if constexpr (PAIR) {
-      next = blockIdx.x >> 1;
-      stride = gridDim.x >> 1;
-      end = (long long)a.num_seqs * a.num_kv_heads * ((a.num_partitions + 1) / 2);
-    } else {
-      uc = cursor_begin(sc, a);
+// ---------------------------------------------------------------- schedule
+// A sequence's units are its query tiles of q_per_unit queries; a chunk
+// longer than the context or than max_query_len (or an invalid length) has
+// none.  q0, q1 = query_start[s], query_start[s + 1].
+__device__ __forceinline__ bool chunk_rows_ok(const DecodeArgs& a, int q0, int q1) {
+  return 0 <= q0 && q0 <= q1 && q1 <= a.num_q_tokens;   // rows inside q / out
+}
+
+__device__ __forceinline__ int prefill_parts(const DecodeArgs& a, int q0, int q1, int L) {
+  const int n = q1 - q0;
+  return (chunk_rows_ok(a, q0, q1) && len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) &&
+          n > 0 && n <= L && n <= a.max_query_len)
+             ? (n + a.q_per_unit - 1) / a.q_per_unit
+             : 0;
+}
+
+// Unit (sequence s, KV head hk, query tile p): its queries and the cache
+// range up to the last one's position; ntiles = 0 when the chunk has no
+// such tile.  Lengths and chunk bounds come from the shared-memory table
+// when it holds them.
+__device__ __forceinline__ UnitInfo unit_at(const Misc& ms, const DecodeArgs& a, int s, int hk,
+                                            int p) {
+  UnitInfo ui;
+  ui.s = s;
+  ui.hk = hk;
+  ui.p = p;
+  ui.slot = -1;
+  const bool tab = a.num_seqs <= kPfTable;
+  ui.L = tab ? ms.tab_L[s] : a.context_lens[s];
+  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
+  const int q0 = tab ? ms.tab_qs[s] : a.query_start[s];
+  const int q1 = tab ? ms.tab_qs[s + 1] : a.query_start[s + 1];
+  if (p < prefill_parts(a, q0, q1, ui.L)) {
+    const int n = q1 - q0, i0 = p * a.q_per_unit;
+    ui.nq = min(a.q_per_unit, n - i0);
+    ui.qrow0 = q0 + i0;
+    ui.pos0 = ui.L - n + i0;
+    ui.t0 = 0;
+    ui.t1 = ui.pos0 + ui.nq;
+    ui.ntiles = (ui.t1 + TT - 1) / TT;
+  } else {
+    ui.ntiles = 0;
+  }
+  return ui;
+}
+
+// The table, and zero rows (with the length status bit) for chunks that
+// cannot be attended: an invalid length, or longer than the context.  Every
+// thread calls this; it ends with __syncthreads().
+__device__ __forceinline__ void prefill_setup(Misc& ms, const DecodeArgs& a) {
+  if (a.num_seqs <= kPfTable)
+    for (int i = threadIdx.x; i <= a.num_seqs; i += kThreads) {
+      if (i < a.num_seqs) ms.tab_L[i] = a.context_lens[i];
+      ms.tab_qs[i] = a.query_start[i];
+    }
+  for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
+    const int L = a.context_lens[sq];
+    const int q0 = a.query_start[sq], q1 = a.query_start[sq + 1], n = q1 - q0;
+    if (!chunk_rows_ok(a, q0, q1)) {     // rows outside q / out: nothing can be written
+      if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
+    } else if (n > 0 && prefill_parts(a, q0, q1, L) == 0) {
+      if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
+      uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)q0 * a.num_heads * a.head_size / 2;
+      const size_t words = (size_t)n * a.num_heads * a.head_size / 2;
+      for (size_t i = threadIdx.x; i < words; i += kThreads) o[i] = 0u;
     }
   }
-  __device__ __forceinline__ bool step(const SchedSmem& sc, const DecodeArgs& a, UnitInfo& ui) {
-    if constexpr (PAIR) {
-      const int PP = (a.num_partitions + 1) / 2;
-      while (next < end) {
-        const int v = (int)next;
-        next += stride;
-        const int pp = PP - 1 - v % PP, sh = v / PP;
-        const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
-        const UnitInfo u0 = prefill_unit_at<TT>(sc, a, s, hk, 2 * pp);
-        const UnitInfo u1 = prefill_unit_at<TT>(sc, a, s, hk, 2 * pp + 1);
+  __syncthreads();
+}
+
+// Units of one CTA, dealt round-robin (consecutive query tiles of a causal
+// chunk differ in cost; dealing spreads them), later (heavier) tiles first.
+// Single form: unit u of S * Hk * P.  Paired form (PAIR): the two CTAs of a
+// cluster take the query tiles 2pp and 2pp + 1 of one (sequence, KV head)
+// together, pairs dealt over the clusters, and both walk the pair's tiles
+// (the longer unit's count), so that every K/V tile is loaded once for both.
+// A CTA whose own tile is absent runs a unit without valid rows, and the
+// shorter unit's extra tiles lie past all of its queries (fully masked).
+template <bool PAIR>
+struct PfCursor {
+  long long next, end;
+  int stride;
+  __device__ __forceinline__ void begin(const DecodeArgs& a) {
+    const long long per = PAIR ? (a.num_partitions + 1) / 2 : a.num_partitions;
+    next = PAIR ? blockIdx.x >> 1 : blockIdx.x;
+    stride = PAIR ? gridDim.x >> 1 : gridDim.x;
+    end = (long long)a.num_seqs * a.num_kv_heads * per;
+  }
+  __device__ __forceinline__ bool step(const Misc& ms, const DecodeArgs& a, UnitInfo& ui) {
+    const int per = PAIR ? (a.num_partitions + 1) / 2 : a.num_partitions;
+    while (next < end) {
+      const int v = (int)next;
+      next += stride;
+      const int pp = per - 1 - v % per, sh = v / per;
+      const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
+      if constexpr (PAIR) {
+        const UnitInfo u0 = unit_at(ms, a, s, hk, 2 * pp);
+        const UnitInfo u1 = unit_at(ms, a, s, hk, 2 * pp + 1);
         if (u0.ntiles == 0 && u1.ntiles == 0) continue;
         ui = cluster_ctarank() ? u1 : u0;
         if (ui.ntiles == 0) {   // no valid rows; q rows read from row 0 (unused)
@@ -120,11 +190,12 @@ struct PfCursor {
         ui.t1 = max(u0.ntiles ? u0.t1 : 0, u1.ntiles ? u1.t1 : 0);
         ui.ntiles = max(u0.ntiles, u1.ntiles);
         return true;
+      } else {
+        ui = unit_at(ms, a, s, hk, pp);
+        if (ui.ntiles) return true;
       }
-      return false;
-    } else {
-      return cursor_next<TT, true>(uc, sc, a, ui);
     }
+    return false;
   }
 };
 
@@ -184,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any multicast
   pdl_wait();
   pdl_launch_dependents();
-  schedule_setup(ms.sched, a, kThreads);
+  prefill_setup(ms, a);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -221,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return raw;
     };
     PfCursor<PAIR> cur;
-    cur.begin(ms.sched, a);
+    cur.begin(a);
     UnitInfo ui;
     // (A warp with no half to load and no barrier to arm has nothing to do.)
-    bool have = (half_mask != 0 || primary) && cur.step(ms.sched, a, ui);
+    bool have = (half_mask != 0 || primary) && cur.step(ms, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -234,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool nhave = true;
       int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nhave = cur.step(ms.sched, a, nui);
+        nhave = cur.step(ms, a, nui);
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
@@ -319,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pv_last) mma_commit(&ms.o_full[ub]);
       };
       PfCursor<PAIR> cur;
-      cur.begin(ms.sched, a);
+      cur.begin(a);
       UnitInfo ui;
-      while (ok && cur.step(ms.sched, a, ui)) {
+      while (ok && cur.step(ms, a, ui)) {
         const int qb = un & 1;
         ok = ok && mbar_wait(&ms.q_full[qb], (un >> 1) & 1);
         for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++j) {
@@ -395,9 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++u_fin;
     };
     PfCursor<PAIR> cur;
-    cur.begin(ms.sched, a);
+    cur.begin(a);
     UnitInfo ui;
-    while (ok && cur.step(ms.sched, a, ui)) {
+    while (ok && cur.step(ms, a, ui)) {
       const int ub = u & 1;
       const bool valid_row = qi < ui.nq;
       const int pos = valid_row ? ui.pos0 + qi : -1;      // last visible token

@@ -16,8 +16,6 @@
 // [T b / G, T (b + 1) / G): a unit is the run of its tiles inside one pair,
 // and only a CTA's first and last units can be cut short (partials in slots
 // 2b and 2b + 1).
-// For prefill a unit is (sequence, KV head, query tile) and reads the cache
-// from token 0 up to the position of the tile's last query.
 #pragma once
 
 #include "common.cuh"
@@ -30,17 +28,16 @@ constexpr int kSchedMax = 1024;
 struct SchedSmem {
   int total;
   int L[kSchedMax];        // context length of each sequence
-  int pre[kSchedMax + 1];  // units (stream: positions) of the sequences before s;
-                           // prefill: query_start
+  int pre[kSchedMax + 1];  // units (stream: positions) of the sequences before s
 };
 
 struct UnitInfo {
   int s, hk, p, L, t0, t1, ntiles;
   bool lok;
   int slot;   // stream form: workspace slot of a partial unit, -1 for a whole one
-  // Prefill only: the unit's queries are chunk queries [p * QT, p * QT + nq)
-  // of sequence s, stored from packed row qrow0 on; the first sits at
-  // position pos0, query c at pos0 + c.
+  // Prefill (its own schedule) only: the unit's queries are chunk queries
+  // [p * QT, p * QT + nq) of sequence s, stored from packed row qrow0 on;
+  // the first sits at position pos0, query c at pos0 + c.
   int qrow0, nq, pos0;
 };
 
@@ -55,67 +52,15 @@ __device__ __forceinline__ int parts_of(const DecodeArgs& a, int L) {
              : 0;
 }
 
-// Prefill: a sequence's units are its query tiles of q_per_unit queries; a
-// chunk longer than the context or than max_query_len (or an invalid
-// length) has none.  q0, q1 = query_start[s], query_start[s + 1].
-__device__ __forceinline__ bool chunk_rows_ok(const DecodeArgs& a, int q0, int q1) {
-  return 0 <= q0 && q0 <= q1 && q1 <= a.num_q_tokens;   // rows inside q / out
-}
-
-__device__ __forceinline__ int prefill_parts(const DecodeArgs& a, int q0, int q1, int L) {
-  const int n = q1 - q0;
-  return (chunk_rows_ok(a, q0, q1) && len_ok(L, a.max_context_len, a.max_blocks_per_seq, a.block_size) &&
-          n > 0 && n <= L && n <= a.max_query_len)
-             ? (n + a.q_per_unit - 1) / a.q_per_unit
-             : 0;
-}
-
-// Token range and queries of prefill unit (s, query tile p): the unit reads
-// the cache up to its last query's position.
 template <int TT>
-__device__ __forceinline__ void prefill_unit(const DecodeArgs& a, int q0, int q1, UnitInfo& ui) {
-  const int n = q1 - q0;
-  const int i0 = ui.p * a.q_per_unit;
-  ui.nq = min(a.q_per_unit, n - i0);
-  ui.qrow0 = q0 + i0;
-  ui.pos0 = ui.L - n + i0;
-  ui.t0 = 0;
-  ui.t1 = ui.pos0 + ui.nq;
-  ui.ntiles = (ui.t1 + TT - 1) / TT;
-}
-
-// Prefill unit (sequence s, KV head hk, query tile p); ntiles = 0 when the
-// chunk has no such tile.  With at most kSchedMax sequences lengths and chunk
-// bounds come from the shared-memory schedule (sc.L, and sc.pre holding
-// query_start).
-template <int TT>
-__device__ __forceinline__ UnitInfo prefill_unit_at(const SchedSmem& sc, const DecodeArgs& a, int s,
-                                                    int hk, int p) {
-  UnitInfo ui;
-  ui.s = s;
-  ui.hk = hk;
-  ui.p = p;
-  ui.slot = -1;
-  const bool smem = a.num_seqs <= kSchedMax;
-  ui.L = smem ? sc.L[s] : a.context_lens[s];
-  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
-  const int q0 = smem ? sc.pre[s] : a.query_start[s];
-  const int q1 = smem ? sc.pre[s + 1] : a.query_start[s + 1];
-  if (p < prefill_parts(a, q0, q1, ui.L)) prefill_unit<TT>(a, q0, q1, ui); else ui.ntiles = 0;
-  return ui;
-}
-
-template <int TT, bool PF>
-__device__ __forceinline__ UnitInfo unit_info(const SchedSmem& sc, const DecodeArgs& a, int u) {
+__device__ __forceinline__ UnitInfo unit_info(const DecodeArgs& a, int u) {
   UnitInfo ui;
   const int P = a.num_partitions;
-  // Prefill: a sequence's later query tiles see more of the cache, so they
-  // are dealt first (heaviest units first, light ones fill the tail).
-  ui.p = PF ? P - 1 - u % P : u % P;
+  ui.p = u % P;
   const int sh = u / P;
   ui.hk = sh % a.num_kv_heads;
   ui.s = sh / a.num_kv_heads;
-  if constexpr (PF) return prefill_unit_at<TT>(sc, a, ui.s, ui.hk, ui.p);
+  ui.slot = -1;
   ui.L = a.context_lens[ui.s];
   ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
   ui.t0 = ui.p * a.partition_size;
@@ -133,9 +78,7 @@ struct UnitCursor {
 
 __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
   UnitCursor c;
-  // Prefill takes units round-robin: consecutive query tiles of a causal
-  // chunk differ in cost, and dealing them across CTAs balances it.
-  c.dense = !a.fused && !a.query_start && a.num_seqs <= kSchedMax;
+  c.dense = !a.fused && a.num_seqs <= kSchedMax;
   c.s = c.hk = c.p = 0;
   c.np = -1;
   if (a.stream) {
@@ -158,11 +101,10 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
   return c;
 }
 
-// PF: prefill units (a.query_start set), else decode units.
-template <int TT, bool PF = false>
+template <int TT>
 __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
                                             const DecodeArgs& a, UnitInfo& ui) {
-  if (a.stream && !PF) {
+  if (a.stream) {
     // Units are the runs of the CTA's range over one pair's tiles; np =
     // positions per pair of sequence s (its tiles and empty positions).
     while (c.next < c.end) {
@@ -250,7 +192,7 @@ __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
     return true;
   }
   while (c.next < c.end) {
-    ui = unit_info<TT, PF>(sc, a, (int)c.next);
+    ui = unit_info<TT>(a, (int)c.next);
     c.next += gridDim.x;
     if (ui.ntiles) return true;
   }
@@ -267,14 +209,7 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
     __syncthreads();
     return;
   }
-  if (a.num_seqs <= kSchedMax && a.query_start) {
-    // Prefill takes units round-robin: the table keeps lengths and chunk
-    // bounds (pre = query_start) for the cursor.
-    for (int i = threadIdx.x; i <= a.num_seqs; i += nthreads) {
-      if (i < a.num_seqs) sc.L[i] = a.context_lens[i];
-      sc.pre[i] = a.query_start[i];
-    }
-  } else if (a.num_seqs <= kSchedMax) {
+  if (a.num_seqs <= kSchedMax) {
     for (int i = threadIdx.x; i < a.num_seqs; i += nthreads) {
       const int L = a.context_lens[i];
       sc.L[i] = L;
@@ -322,24 +257,6 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
         a.ws_desc[blockIdx.x] = d;
       }
     }
-  }
-  if (a.query_start) {
-    // Prefill: zero the query rows of chunks that cannot be attended (an
-    // invalid length, or longer than the context) and flag them.
-    for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
-      const int L = a.context_lens[sq];
-      const int q0 = a.query_start[sq], q1 = a.query_start[sq + 1], n = q1 - q0;
-      if (!chunk_rows_ok(a, q0, q1)) {     // rows outside q / out: nothing can be written
-        if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
-      } else if (n > 0 && prefill_parts(a, q0, q1, L) == 0) {
-        if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
-        uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)q0 * a.num_heads * a.head_size / 2;
-        const size_t words = (size_t)n * a.num_heads * a.head_size / 2;
-        for (size_t i = threadIdx.x; i < words; i += nthreads) o[i] = 0u;
-      }
-    }
-    __syncthreads();
-    return;
   }
   for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
     const int L = a.num_seqs <= kSchedMax ? sc.L[sq] : a.context_lens[sq];
