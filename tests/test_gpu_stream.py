@@ -81,6 +81,26 @@ def test_stream_matches_oracle_and_partition_form(H, Hk, B, dtype, kind):
     assert np.abs(got - got2).max() <= 2e-2
 
 
+def test_stream_at_its_sequence_limit():
+    # 1024 sequences (the most the in-kernel prefix holds), lengths 0..300:
+    # many pairs per share, every kind of range edge; sampled rows.
+    from .gpu_util import sample_pairs
+    rng = np.random.default_rng(131)
+    lens = [int(L) for L in rng.integers(0, 301, 1024)]
+    lens[:3] = [0, 1, 300]
+    c = _case(137, 32, 4, 16, lens, "bf16")
+    from paged_kv_decode_22_gb300 import ops
+    assert _plan(c, STREAM)[2] == ops.PATH_TC_STREAM
+    got, status = run_decode(DeviceCase(c), partition_size=STREAM)
+    assert status == 0
+    pairs = sample_pairs(c, 96, seed=3)
+    ref = _oracle(c, pairs=pairs)
+    assert_close(np.stack([got[s_, h] for s_, h in pairs]), ref, "1024 sequences, stream form")
+    for s_, L in enumerate(lens):
+        if L == 0:
+            assert (got[s_] == 0).all()
+
+
 def test_stream_is_repeatable():
     c = _case(107, 64, 8, 16, _lens("many", 8), "bf16")
     dc = DeviceCase(c)
