@@ -85,8 +85,8 @@ __global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(const DecodeArg
 // when its last tile is partial), CTA b held [T b / G, T (b + 1) / G).  A pair
 // cut by a range edge left partials: CTA b0 (holding position A; the pair
 // begins inside its range) in slot 2 b0 + 1, and every later CTA up to b1
-// (holding A + n - 1) whose range is not empty in slot 2b.  One
-// column of blocks per range edge (16 heads per block, a warp per head); the
+// (holding A + n - 1) whose range is not empty in slot 2b.  One column of
+// blocks per range edge (kMergeWarps heads per block, a warp per head); the
 // column of the pair's first cut (b0 + 1) merges it.
 constexpr int kMergeWarps = 8;
 constexpr int kMergeChunk = 8;    // partial slots loaded at once
