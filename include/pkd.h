@@ -280,6 +280,19 @@ PKD_API pkd_status pkd_reshape_and_cache(const void* key, const void* value, voi
                                  int num_heads, int head_size, int block_size, int num_blocks,
                                  pkd_dtype dtype, uint32_t* device_status, void* stream);
 
+/*
+ * Self-test of failure detection without a GPU fault.  Every kernel's waits
+ * are bounded: a wait that gives up ORs PKD_DEV_TIMEOUT into device_status
+ * and the kernel returns.  This launches one thread that waits, through that
+ * same routine, on a shared-memory barrier nothing arrives on, for limit_ns
+ * nanoseconds (1e3 .. 1e9); it then sets PKD_DEV_TIMEOUT in *device_status
+ * (a device uint32_t) and returns, leaving the context usable.  Host
+ * errors: PKD_ERR_NULL without device_status, PKD_ERR_SHAPE for a limit out
+ * of range, both before any launch.
+ */
+PKD_API pkd_status pkd_selftest_bounded_wait(uint32_t* device_status, long long limit_ns,
+                                             void* stream);
+
 /* Static text for a status code. */
 PKD_API const char* pkd_status_string(pkd_status status);
 

@@ -37,6 +37,7 @@ _SIGS = {
                                     [_c_float, _vp, _c_int, _vp, _vp]),
     "pkd_gather_cached_kv": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_vp, _vp]),
     "pkd_reshape_and_cache": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_vp, _vp]),
+    "pkd_selftest_bounded_wait": (_c_int, [_vp, ctypes.c_longlong, _vp]),
     "pkd_status_string": (ctypes.c_char_p, [_c_int]),
     "pkd_last_error": (ctypes.c_char_p, []),
     "pkd_version": (_c_int, []),

@@ -296,6 +296,16 @@ pkd_status pkd_paged_decode_attention_ex(void* out, const void* q, const void* k
   return PKD_OK;
 }
 
+pkd_status pkd_selftest_bounded_wait(uint32_t* device_status, long long limit_ns, void* stream) {
+  if (!device_status) return PKD_ERR_NULL;
+  if (limit_ns < 1000 || limit_ns > 1000000000LL) return PKD_ERR_SHAPE;
+  DeviceInfo dev;
+  pkd_status st = device_info(&dev);
+  if (st != PKD_OK) return st;
+  cudaError_t e = pkd::launch_selftest_wait(device_status, limit_ns, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKD_OK : cuda_fail(e, "self-test launch");
+}
+
 pkd_status pkd_paged_prefill_attention(void* out, const void* q, const void* key_cache,
                                        const void* value_cache, const int32_t* block_tables,
                                        int max_blocks_per_seq, const int32_t* context_lens,

@@ -119,6 +119,7 @@ cudaError_t launch_prefill_rows(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_lse_reduce(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_stream_merge(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st);
+cudaError_t launch_selftest_wait(uint32_t* status, long long limit_ns, cudaStream_t st);
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st);
 
 }  // namespace pkd

@@ -44,6 +44,12 @@ def test_header_constants_match_the_binding():
         assert defs.get(name) == value, (name, defs.get(name), value)
 
 
+def test_selftest_rejects_bad_arguments_on_host(lib):
+    assert lib.pkd_selftest_bounded_wait(NULL, 1000000, NULL) == 1
+    assert lib.pkd_selftest_bounded_wait(FAKE, 10, NULL) == 2
+    assert lib.pkd_selftest_bounded_wait(FAKE, 2 * 10**9, NULL) == 2
+
+
 def test_version_and_status_strings(lib):
     assert lib.pkd_version() >= 100
     for code in range(8):
