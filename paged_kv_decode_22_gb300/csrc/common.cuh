@@ -35,12 +35,33 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // Programmatic dependent launch.  Every kernel is launched so that the next
 // kernel in the stream may start while its CTAs drain; each kernel therefore
-// waits, before its first global-memory access, until the previous grid has
-// completed and its writes are visible, and then lets its own dependents
-// launch.  Without the launch attribute both instructions do nothing.
+// waits, before its first global-memory read or write (L2 prefetches, which
+// read nothing, may come earlier), until the previous grid has completed and
+// its writes are visible, and then lets its own dependents launch.  Without
+// the launch attribute both instructions do nothing.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Asks L2 for the cache lines of the byte range [base, base + bytes): the
+// lines first, first + step, first + 2 step, ... of the range, at most
+// `count` of them, spread over the CTA's threads.  A prefetch reads no value
+// into the SM, so it may be issued before pdl_wait(): the lines are then on
+// their way while the previous grid drains, and a later load still sees that
+// grid's writes, which are made in L2.  Every address lies inside the range.
+__device__ __forceinline__ void prefetch_l2_lines(const void* base, size_t bytes, long long first,
+                                                  long long step, int count) {
+  if (bytes == 0) return;
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  const uintptr_t start = b & ~uintptr_t(127);
+  const long long lines = (long long)((b + bytes - start + 127) / 128);
+  for (int k = threadIdx.x; k < count; k += blockDim.x) {
+    const long long l = first + (long long)k * step;
+    if (l >= lines) break;
+    const uintptr_t p = l == 0 ? b : start + (uintptr_t)l * 128;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+  }
 }
 
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) {

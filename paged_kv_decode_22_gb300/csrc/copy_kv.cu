@@ -37,6 +37,7 @@ __device__ __forceinline__ void copy_row(char* dst, const char* src, int n16) {
 }
 
 __global__ void __launch_bounds__(kThreads) gather_kernel(const CopyArgs a) {
+  prefetch_l2_lines(a.slots + blockIdx.x, 8, 0, 1, 1);   // this CTA's slot, while the previous grid drains
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const CopyArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) scatter_kernel(const CopyArgs a) {
+  prefetch_l2_lines(a.slots + blockIdx.x, 8, 0, 1, 1);   // this CTA's slot, while the previous grid drains
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;

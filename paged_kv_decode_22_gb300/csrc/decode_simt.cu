@@ -167,6 +167,14 @@ __global__ void __launch_bounds__(kThreads)
   const int t0 = p * a.partition_size;
   const int32_t* bt = a.block_tables + (size_t)s * a.max_blocks_per_seq;
 
+  const int tab_tokens = a.max_blocks_per_seq << lb;
+  const int blk_first = t0 >> lb;   // first block of the partition
+  const int blk_end = t0 < tab_tokens ? ((min(t0 + a.partition_size, tab_tokens) - 1) >> lb) + 1 : blk_first;
+  const uint16_t* qp0 = reinterpret_cast<const uint16_t*>(a.q) + ((size_t)s * H + h0) * D;
+  // The entry loads below, requested into L2 while the previous grid drains.
+  prefetch_l2_lines(a.context_lens + s, 4, 0, 1, 1);
+  prefetch_l2_lines(bt + blk_first, (size_t)min(blk_end - blk_first, kMaxIds) * 4, 0, 1, kThreads);
+  prefetch_l2_lines(qp0, (size_t)GC * D * 2, 0, 1, kThreads);
   if (threadIdx.x == 0) {
     for (int w = 0; w < kWarps; ++w)
       for (int i = 0; i < kStages; ++i) mbar_init(&full[w][i], 1);
@@ -176,9 +184,6 @@ __global__ void __launch_bounds__(kThreads)
   pdl_launch_dependents();
   // ---- entry: length, block ids of this partition (first pass) and q together
   const int L = a.context_lens[s];
-  const int tab_tokens = a.max_blocks_per_seq << lb;
-  const int blk_first = t0 >> lb;   // first block of the partition
-  const int blk_end = t0 < tab_tokens ? ((min(t0 + a.partition_size, tab_tokens) - 1) >> lb) + 1 : blk_first;
   {
     const int n = min(blk_end - blk_first, kMaxIds);
     for (int i = threadIdx.x; i < n; i += kThreads) ids[i] = __ldg(bt + blk_first + i);
@@ -187,8 +192,7 @@ __global__ void __launch_bounds__(kThreads)
   const float qscale = a.scale * kLog2e;
   uint4 qw[GC];
   {
-    const uint16_t* qp =
-        reinterpret_cast<const uint16_t*>(a.q) + ((size_t)s * H + h0) * D + part * 8;
+    const uint16_t* qp = qp0 + part * 8;
 #pragma unroll
     for (int j = 0; j < GC; ++j) qw[j] = *reinterpret_cast<const uint4*>(qp + (size_t)j * D);
   }

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   const int g = a.num_heads / a.num_kv_heads;
 
   // ---------------------------------------------------------------- setup
+  prefetch_schedule_inputs(a);
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) {
       mbar_init(&ms.k_full[i], 1);

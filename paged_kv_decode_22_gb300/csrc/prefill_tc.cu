@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kMmaCount = PAIR ? 2 : 1;
 
   // ---------------------------------------------------------------- setup
+  prefetch_schedule_inputs(a);
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) {
       mbar_init(&ms.k_full[i], 1);

@@ -199,6 +199,33 @@ __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
   return false;
 }
 
+// L2 prefetch, issued before pdl_wait(), of what a persistent kernel reads
+// first: the context lengths (all of them when every CTA builds the
+// schedule, else a share) and, in the persistent forms, the used head of
+// every block-table row (ceil(max_context_len / block_size) entries), row s
+// by CTA s mod G; in the cluster form the CTA's own length and partition.
+__device__ __forceinline__ void prefetch_schedule_inputs(const DecodeArgs& a) {
+  const int S = a.num_seqs, B = a.block_size, mbps = a.max_blocks_per_seq;
+  if (a.fused) {
+    const int s = blockIdx.y / a.num_kv_heads;
+    const long long b0 = (long long)blockIdx.x * a.partition_size / B;
+    prefetch_l2_lines(a.context_lens + s, 4, 0, 1, 1);
+    if (b0 < mbps) {
+      const long long nb = min((long long)(a.partition_size + B - 1) / B + 1, (long long)mbps - b0);
+      prefetch_l2_lines(a.block_tables + (size_t)s * mbps + b0, (size_t)nb * 4, 0, 1, 64);
+    }
+    return;
+  }
+  if (S <= kSchedMax)
+    prefetch_l2_lines(a.context_lens, (size_t)S * 4, 0, 1, 64);
+  else
+    prefetch_l2_lines(a.context_lens, (size_t)S * 4, blockIdx.x, gridDim.x, 64);
+  if (a.query_start) prefetch_l2_lines(a.query_start, (size_t)(S + 1) * 4, 0, 1, 64);
+  const long long used = min((long long)mbps, ((long long)a.max_context_len + B - 1) / B);
+  for (int s = blockIdx.x; s < S; s += gridDim.x)
+    prefetch_l2_lines(a.block_tables + (size_t)s * mbps, (size_t)used * 4, 0, 1, 1024);
+}
+
 // Build the schedule (when dense) and zero the output rows of sequences that
 // have nothing to attend to (unsplit plans; the merge writes them when
 // split), setting the length status bit for invalid lengths.  Every thread
