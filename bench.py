@@ -52,11 +52,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # the sha256 (first 16 hex digits) of the kernel source it was taken on; the
 # value is reported only while that source is unchanged.
 NCU_TRAFFIC = {
-    # gather_t2048, profiles/gather_cached_kv_t2048.md: 41.97 MB read + 1.70 MB
+    # gather_t2048, profiles/gather_cached_kv_t2048.md: 41.97 MB read + 1.80 MB
     # written during the kernel (its output is still dirty in L2 when it ends)
-    "256628f9b483485a": 43661824,
+    "1728429f21e5a968": 41969152 + 1797376,
     # llama13b_mha_b8_ctx256, profiles/decode_simt_llama13b_mha_b8_ctx256.md
-    "4a694aac59655cca": 42099968,
+    "90c0e845acbd2fec": 42051328 + 56576,
 }
 
 
