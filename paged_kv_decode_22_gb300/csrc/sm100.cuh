@@ -161,6 +161,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* tmap, ui
       : "memory");
 }
 
+// Bulk copy global -> shared (no tensor map), completing on `bar` with its
+// byte count.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Bulk copy shared -> global (no tensor map), tracked by bulk groups.
 // Addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {

@@ -36,8 +36,12 @@ def test_gather_sweep_bit_exact(name):
     np.testing.assert_array_equal(v, rv)
 
 
+# 50 tokens are 100 rows: rows of 16 B up to 32 KB take the bulk-copy kernel
+# (128 x 128 x 2 B is its largest row); 136 heads give 34 KB rows, which take
+# the 16-byte-load kernel, as do the sweep's gathers of more than 512 tokens.
 @pytest.mark.parametrize("H,D,B,dtype", [(1, 8, 1, "fp16"), (3, 24, 5, "bf16"),
-                                         (8, 128, 16, "bf16"), (40, 128, 8, "fp16")])
+                                         (8, 128, 16, "bf16"), (40, 128, 8, "fp16"),
+                                         (128, 128, 4, "bf16"), (136, 128, 2, "fp16")])
 def test_gather_odd_shapes_and_invalid_slots(H, D, B, dtype):
     g = make_gather_case(seed=4, num_tokens=50, num_heads=H, head_size=D, block_size=B,
                          num_blocks=64, dtype=dtype)
