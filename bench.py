@@ -54,7 +54,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 NCU_TRAFFIC = {
     # gather_t2048, profiles/gather_cached_kv_t2048.md: 41.97 MB read + 1.80 MB
     # written during the kernel (its output is still dirty in L2 when it ends)
-    "7fb3b6da36c6336c": 41969152 + 1797376,
+    "aba4662af3507d10": 41969152 + 1797376,
     # llama13b_mha_b8_ctx256, profiles/decode_simt_llama13b_mha_b8_ctx256.md
     "90c0e845acbd2fec": 42051328 + 56576,
 }

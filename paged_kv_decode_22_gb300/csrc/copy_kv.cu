@@ -10,13 +10,15 @@
 // plain row copies.  One CTA copies one token's K row (blockIdx.y = 0) or V
 // row (blockIdx.y = 1).
 //
-// Gather of at most kBulkMaxRows rows of up to 32 KB: a one-warp CTA whose
+// Copies of at most kBulkMaxRows rows of up to 32 KB: a one-warp CTA whose
 // first lane moves the row with two bulk copies, global -> shared
-// (completing on an mbarrier) and shared -> global.  Everything else
-// (scatter, more rows, larger rows): 16-byte streaming loads and stores, five
-// in flight per thread (a 40-head x 128 row of 640 chunks is one round of 128
-// threads).  Measured on 40 x 128 fp16 rows: bulk is 19-31 % faster up to
-// 512 rows (T <= 256), equal at 1024 and 4096 rows, and 8 % slower at 2048.
+// (completing on an mbarrier) and shared -> global.  More rows, or larger
+// ones: 16-byte streaming loads and stores, five in flight per thread (a
+// 40-head x 128 row of 640 chunks is one round of 128 threads).  Measured on
+// 40 x 128 fp16 rows, bulk against 16-byte loads: 19-31 % (gather) and
+// 12-22 % (scatter) faster up to 512 rows (T <= 256); at 1024 rows equal
+// (gather) and 3 % slower (scatter); at 2048 rows 8-11 % slower; at 4096
+// equal.
 #include "common.cuh"
 #include "internal.h"
 #include "sm100.cuh"
@@ -63,13 +65,17 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const CopyArgs a) {
   copy_row(dst, src, n16);
 }
 
-// Gathers of at most kBulkMaxRows rows of at most kBulkRowMax bytes go
+// Copies of at most kBulkMaxRows rows of at most kBulkRowMax bytes go
 // through shared memory by bulk copies (a row within the default 48 KB of
 // dynamic shared memory).
 constexpr uint32_t kBulkRowMax = 32 * 1024;
-constexpr long long kBulkMaxRows = 1024;
+constexpr long long kBulkMaxRows = 512;
 
-__global__ void __launch_bounds__(32) gather_bulk_kernel(const CopyArgs a) {
+// One row per one-warp CTA, in the direction SCATTER names; slots outside the
+// pool are handled as in gather_kernel (zero row, status bit) and
+// scatter_kernel (negative: padding, skipped; past the pool: status bit).
+template <bool SCATTER>
+__global__ void __launch_bounds__(32) copy_bulk_kernel(const CopyArgs a) {
   extern __shared__ __align__(128) uint8_t row_buf[];
   __shared__ uint64_t bar;
   prefetch_l2_lines(a.slots + blockIdx.x, 8, 0, 1, 1);   // this CTA's slot, while the previous grid drains
@@ -83,15 +89,20 @@ __global__ void __launch_bounds__(32) gather_bulk_kernel(const CopyArgs a) {
   const int t = blockIdx.x;
   const bool is_v = blockIdx.y != 0;
   const uint32_t row_bytes = (uint32_t)a.row_elems * 2;
-  char* dst = static_cast<char*>(is_v ? a.dst_v : a.dst_k) + (size_t)t * row_bytes;
   const long long slot = a.slots[t];
   if (slot < 0 || slot >= (long long)a.num_blocks * a.block_size) {
-    for (uint32_t i = threadIdx.x; i < row_bytes / 16; i += 32)
-      st_stream(dst + (size_t)i * 16, make_uint4(0, 0, 0, 0));
-    if (!is_v && threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_SLOT);
+    if constexpr (!SCATTER) {
+      char* dst = static_cast<char*>(is_v ? a.dst_v : a.dst_k) + (size_t)t * row_bytes;
+      for (uint32_t i = threadIdx.x; i < row_bytes / 16; i += 32)
+        st_stream(dst + (size_t)i * 16, make_uint4(0, 0, 0, 0));
+    }
+    if (!is_v && threadIdx.x == 0 && (!SCATTER || slot >= 0)) flag(a.status, PKD_DEV_BAD_SLOT);
     return;
   }
-  const char* src = static_cast<const char*>(is_v ? a.src_v : a.src_k) + (size_t)slot * row_bytes;
+  const size_t src_row = SCATTER ? (size_t)t : (size_t)slot;
+  const size_t dst_row = SCATTER ? (size_t)slot : (size_t)t;
+  const char* src = static_cast<const char*>(is_v ? a.src_v : a.src_k) + src_row * row_bytes;
+  char* dst = static_cast<char*>(is_v ? a.dst_v : a.dst_k) + dst_row * row_bytes;
   if (threadIdx.x == 0) {
     sm100::mbar_arrive_expect_tx(&bar, row_bytes);
     sm100::bulk_load(row_buf, src, row_bytes, &bar);
@@ -104,6 +115,10 @@ __global__ void __launch_bounds__(32) gather_bulk_kernel(const CopyArgs a) {
       sm100::mbar_wait(&bar, 0, 100000000ull);   // let the load land before the CTA exits
     }
   }
+}
+
+bool bulk_fits(const CopyArgs& a) {
+  return (uint32_t)a.row_elems * 2 <= kBulkRowMax && 2LL * a.num_tokens <= kBulkMaxRows;
 }
 
 __global__ void __launch_bounds__(kThreads) scatter_kernel(const CopyArgs a) {
@@ -128,13 +143,16 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const CopyArgs a) {
 }  // namespace
 
 cudaError_t launch_gather(const CopyArgs& a, cudaStream_t st) {
-  const uint32_t row_bytes = (uint32_t)a.row_elems * 2;
-  if (row_bytes <= kBulkRowMax && 2LL * a.num_tokens <= kBulkMaxRows)
-    return launch_pdl(gather_bulk_kernel, dim3(a.num_tokens, 2), dim3(32), row_bytes, st, a);
+  if (bulk_fits(a))
+    return launch_pdl(copy_bulk_kernel<false>, dim3(a.num_tokens, 2), dim3(32),
+                      (size_t)a.row_elems * 2, st, a);
   return launch_pdl(gather_kernel, dim3(a.num_tokens, 2), dim3(kThreads), 0, st, a);
 }
 
 cudaError_t launch_scatter(const CopyArgs& a, cudaStream_t st) {
+  if (bulk_fits(a))
+    return launch_pdl(copy_bulk_kernel<true>, dim3(a.num_tokens, 2), dim3(32),
+                      (size_t)a.row_elems * 2, st, a);
   return launch_pdl(scatter_kernel, dim3(a.num_tokens, 2), dim3(kThreads), 0, st, a);
 }
 

@@ -38,7 +38,7 @@ def test_gather_sweep_bit_exact(name):
 
 # 50 tokens are 100 rows: rows of 16 B up to 32 KB take the bulk-copy kernel
 # (128 x 128 x 2 B is its largest row); 136 heads give 34 KB rows, which take
-# the 16-byte-load kernel, as do the sweep's gathers of more than 512 tokens.
+# the 16-byte-load kernel, as do the sweep's gathers of more than 256 tokens.
 @pytest.mark.parametrize("H,D,B,dtype", [(1, 8, 1, "fp16"), (3, 24, 5, "bf16"),
                                          (8, 128, 16, "bf16"), (40, 128, 8, "fp16"),
                                          (128, 128, 4, "bf16"), (136, 128, 2, "fp16")])
@@ -61,16 +61,18 @@ def test_gather_empty_is_a_no_op():
     assert k.shape == (0, 2, 8) and status == 0
 
 
+# 200 tokens (400 rows) take the bulk-copy kernel, 700 the 16-byte-load one.
+@pytest.mark.parametrize("T", [200, 700])
 @pytest.mark.parametrize("H,D,B,dtype", [(40, 128, 8, "fp16"), (8, 128, 16, "bf16"),
                                          (3, 16, 3, "fp16")])
-def test_reshape_and_cache_bit_exact(H, D, B, dtype):
+def test_reshape_and_cache_bit_exact(H, D, B, dtype, T):
     from paged_kv_decode_22_gb300 import ops
-    nb = max(64, -(-400 // B))
-    g = make_gather_case(seed=6, num_tokens=300, num_heads=H, head_size=D, block_size=B,
+    nb = max(64, -(-(T + 100) // B))
+    g = make_gather_case(seed=6, num_tokens=T, num_heads=H, head_size=D, block_size=B,
                          num_blocks=nb, dtype=dtype)
     rng = np.random.default_rng(2)
-    key = rng.integers(0, 0x7C00, (300, H, D), dtype=np.uint16)   # finite fp16/bf16 patterns
-    val = rng.integers(0, 0x7C00, (300, H, D), dtype=np.uint16)
+    key = rng.integers(0, 0x7C00, (T, H, D), dtype=np.uint16)   # finite fp16/bf16 patterns
+    val = rng.integers(0, 0x7C00, (T, H, D), dtype=np.uint16)
     slots = g.slot_mapping.copy()
     slots[[0, 5]] = [-1, nb * B + 2]
     kc, vc = up(g.key_cache, dtype), up(g.value_cache, dtype)
