@@ -61,6 +61,34 @@ def test_gather_empty_is_a_no_op():
     assert k.shape == (0, 2, 8) and status == 0
 
 
+@pytest.mark.parametrize("T", [256, 257])
+def test_copies_at_the_kernel_boundary(T):
+    # 256 tokens (512 rows) are the most the bulk-copy kernel takes; 257 go
+    # to the 16-byte-load kernels.  Both directions, with a bad slot each.
+    from paged_kv_decode_22_gb300 import ops
+    g = make_gather_case(seed=9, num_tokens=T, num_heads=40, head_size=128, block_size=8,
+                         num_blocks=64, dtype="fp16")
+    slots = g.slot_mapping.copy()
+    slots[T - 1] = 64 * 8 + 1
+    k, v, status = _run_gather(g, slots)
+    rk, rv = oracle_gather(g.key_cache, g.value_cache, slots)
+    assert status == 2
+    np.testing.assert_array_equal(k, rk)
+    np.testing.assert_array_equal(v, rv)
+    rng = np.random.default_rng(T)
+    key = rng.integers(0, 0x7C00, (T, 40, 128), dtype=np.uint16)
+    val = rng.integers(0, 0x7C00, (T, 40, 128), dtype=np.uint16)
+    slots[0] = -1
+    kc, vc = up(g.key_cache, "fp16"), up(g.value_cache, "fp16")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.reshape_and_cache(up(key, "fp16"), up(val, "fp16"), kc, vc, up(slots), device_status=st)
+    torch.cuda.synchronize()
+    rk, rv = cache_kv(key, val, g.key_cache, g.value_cache, slots)
+    assert int(st.item()) == 2
+    np.testing.assert_array_equal(down_bits(kc), rk)
+    np.testing.assert_array_equal(down_bits(vc), rv)
+
+
 # 200 tokens (400 rows) take the bulk-copy kernel, 700 the 16-byte-load one.
 @pytest.mark.parametrize("T", [200, 700])
 @pytest.mark.parametrize("H,D,B,dtype", [(40, 128, 8, "fp16"), (8, 128, 16, "bf16"),
