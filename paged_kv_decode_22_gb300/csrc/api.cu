@@ -3,8 +3,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/pkd.h"
 #include "internal.h"
@@ -25,22 +27,30 @@ struct DeviceInfo {
   int minor = 0;
 };
 
-// Per-device attributes, queried once per device and cached.
+// Per-device attributes, queried once per device and cached (the first
+// query is made under a lock; later calls read the cache after an acquire
+// load of its ready flag).
 pkd_status device_info(DeviceInfo* out) {
   static DeviceInfo cache[64];
+  static std::atomic<bool> ready[64];
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return PKD_ERR_DEVICE;
-  DeviceInfo& d = cache[dev];
-  if (d.sms == 0) {
-    DeviceInfo n;
-    if ((e = cudaDeviceGetAttribute(&n.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&n.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&n.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
-      return cuda_fail(e, "cudaDeviceGetAttribute");
-    d = n;
+  if (!ready[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev].load(std::memory_order_relaxed)) {
+      DeviceInfo n;
+      if ((e = cudaDeviceGetAttribute(&n.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&n.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&n.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+      cache[dev] = n;
+      ready[dev].store(true, std::memory_order_release);
+    }
   }
+  const DeviceInfo& d = cache[dev];
   *out = d;
   if (d.major != 10 || d.minor != 3) return PKD_ERR_DEVICE;  // built for sm_103a only
   return PKD_OK;

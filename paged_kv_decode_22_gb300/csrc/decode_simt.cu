@@ -44,6 +44,8 @@
 // writes the unnormalised partial (o, m, l) that lse_reduce.cu merges.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "sm100.cuh"
@@ -420,14 +422,14 @@ __global__ void __launch_bounds__(kThreads)
 template <bool BF16, int D, int GC>
 cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
                      cudaStream_t st) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // setting it twice from two threads is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<BF16, D, GC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<D>::bytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int g = a.num_heads / a.num_kv_heads;
   dim3 grid(a.num_partitions, a.num_kv_heads * (g / GC), a.num_seqs);

@@ -38,6 +38,8 @@
 // launch.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "schedule.cuh"
@@ -711,17 +713,17 @@ template <bool BF16, int NPAD>
 cudaError_t prepare(int* smem_out) {
   const int smem = SmemLayout<NPAD>::bytes + 1024;
   *smem_out = smem;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // setting it twice from two threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || attr_set[dev]) return cudaSuccess;
+  if (dev < 0 || dev >= 64 || attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
   if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
     return e;
-  attr_set[dev] = true;
+  attr_set[dev].store(true, std::memory_order_release);
   return cudaSuccess;
 }
 
@@ -774,11 +776,11 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
 // Co-resident clusters of `cluster` CTAs, cached per device and cluster size.
 template <int NPAD>
 int capacity_t(int cluster) {
-  static int cache[64][kMaxCluster + 1];   // value + 1; 0 = not yet queried
+  static std::atomic<int> cache[64][kMaxCluster + 1];   // value + 1; 0 = not yet queried
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  int& c = cache[dev][cluster];
-  if (c == 0) {
+  std::atomic<int>& c = cache[dev][cluster];
+  if (c.load(std::memory_order_relaxed) == 0) {
     int smem = 0, n = 0;
     if (prepare<true, NPAD>(&smem) == cudaSuccess) {
       cudaLaunchConfig_t cfg;
@@ -790,9 +792,9 @@ int capacity_t(int cluster) {
         n = 0;
       }
     }
-    c = n + 1;
+    c.store(n + 1, std::memory_order_relaxed);
   }
-  return c - 1;
+  return c.load(std::memory_order_relaxed) - 1;
 }
 
 template <bool BF16>

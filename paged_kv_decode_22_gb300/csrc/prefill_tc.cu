@@ -35,6 +35,8 @@
 // Stage release counts both CTAs' MMA commits (multicast tcgen05.commit).
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "schedule.cuh"
@@ -613,15 +615,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Maximum dynamic shared memory, set once per device and kernel.
 template <bool BF16, bool PAIR>
 cudaError_t prepare() {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // setting it twice from two threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<BF16, PAIR>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }
@@ -647,10 +649,10 @@ void pair_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&attr)[2], int gr
 // none, the single form is used).
 template <bool BF16>
 int pair_capacity() {
-  static int cache[64];   // value + 1; 0 = not yet queried
+  static std::atomic<int> cache[64];   // value + 1; 0 = not yet queried
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
+  if (cache[dev].load(std::memory_order_relaxed) == 0) {
     int n = 0;
     if (prepare<BF16, true>() == cudaSuccess) {
       cudaLaunchConfig_t cfg;
@@ -661,9 +663,9 @@ int pair_capacity() {
         n = 0;
       }
     }
-    cache[dev] = n + 1;
+    cache[dev].store(n + 1, std::memory_order_relaxed);
   }
-  return cache[dev] - 1;
+  return cache[dev].load(std::memory_order_relaxed) - 1;
 }
 
 template <bool BF16>
