@@ -2,7 +2,7 @@
 
 The launch code keeps per-device host state that the first call of each
 kernel sets: shared-memory size attributes, cluster and pair capacities,
-device attributes.  Six threads make their first calls together, each on its
+device attributes.  Seven threads make their first calls together, each on its
 own stream and each through a different kernel.  The kernels are CUDA-core
 decode, tensor-core decode, stream form, cluster form, paired prefill, and
 bulk and 16-byte gathers.  Every output and status word must equal, bit for
