@@ -27,12 +27,6 @@
 //              columns of the tile's S buffer, the A operand of P V.
 // TMEM: S double-buffered (2 x 128 columns), O double-buffered by unit
 // parity (2 x 128), 512 columns.
-//
-// Paired form (chunks of several query tiles, g >= 2): a cluster of two CTAs
-// takes two query tiles of one (sequence, KV head) in lockstep; rank r loads
-// the 64-column half r of each K and V tile, TMA-multicast into both CTAs, so
-// each SM issues half the boxes and a tile's boxes leave two SMs at once.
-// Stage release counts both CTAs' MMA commits (multicast tcgen05.commit).
 #include <cuda.h>
 
 #include <atomic>
@@ -153,55 +147,32 @@ __device__ __forceinline__ void prefill_setup(Misc& ms, const DecodeArgs& a) {
   __syncthreads();
 }
 
-// Units of one CTA, dealt round-robin (consecutive query tiles of a causal
-// chunk differ in cost; dealing spreads them), later (heavier) tiles first.
-// Single form: unit u of S * Hk * P.  Paired form (PAIR): the two CTAs of a
-// cluster take the query tiles 2pp and 2pp + 1 of one (sequence, KV head)
-// together, pairs dealt over the clusters, and both walk the pair's tiles
-// (the longer unit's count), so that every K/V tile is loaded once for both.
-// A CTA whose own tile is absent runs a unit without valid rows, and the
-// shorter unit's extra tiles lie past all of its queries (fully masked).
-template <bool PAIR>
+// Units of one CTA: unit u of S * Hk * P, dealt round-robin (consecutive
+// query tiles of a causal chunk differ in cost; dealing spreads them), later
+// (heavier) tiles first.
 struct PfCursor {
   long long next, end;
   int stride;
   __device__ __forceinline__ void begin(const DecodeArgs& a) {
-    const long long per = PAIR ? (a.num_partitions + 1) / 2 : a.num_partitions;
-    next = PAIR ? blockIdx.x >> 1 : blockIdx.x;
-    stride = PAIR ? gridDim.x >> 1 : gridDim.x;
-    end = (long long)a.num_seqs * a.num_kv_heads * per;
+    next = blockIdx.x;
+    stride = gridDim.x;
+    end = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   }
   __device__ __forceinline__ bool step(const Misc& ms, const DecodeArgs& a, UnitInfo& ui) {
-    const int per = PAIR ? (a.num_partitions + 1) / 2 : a.num_partitions;
+    const int per = a.num_partitions;
     while (next < end) {
       const int v = (int)next;
       next += stride;
       const int pp = per - 1 - v % per, sh = v / per;
       const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
-      if constexpr (PAIR) {
-        const UnitInfo u0 = unit_at(ms, a, s, hk, 2 * pp);
-        const UnitInfo u1 = unit_at(ms, a, s, hk, 2 * pp + 1);
-        if (u0.ntiles == 0 && u1.ntiles == 0) continue;
-        ui = cluster_ctarank() ? u1 : u0;
-        if (ui.ntiles == 0) {   // no valid rows; q rows read from row 0 (unused)
-          ui.nq = 0;
-          ui.qrow0 = 0;
-          ui.pos0 = 0;
-          ui.t0 = 0;
-        }
-        ui.t1 = max(u0.ntiles ? u0.t1 : 0, u1.ntiles ? u1.t1 : 0);
-        ui.ntiles = max(u0.ntiles, u1.ntiles);
-        return true;
-      } else {
-        ui = unit_at(ms, a, s, hk, pp);
-        if (ui.ntiles) return true;
-      }
+      ui = unit_at(ms, a, s, hk, pp);
+      if (ui.ntiles) return true;
     }
     return false;
   }
 };
 
-template <bool BF16, bool PAIR>
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
@@ -216,12 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = a.num_heads / a.num_kv_heads;
-  // Paired form: each CTA loads half of every K and V tile into both CTAs of
-  // the cluster; a stage is free once the MMAs of both CTAs are done with it (and, for K,
-  // this CTA's softmax has read the stage's bad-block entry: without that
-  // arrival a stage could be refilled twice before the softmax checks it).
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
-  constexpr uint32_t kMmaCount = PAIR ? 2 : 1;
+  // A K stage is free once the MMA is done with it and the softmax has read
+  // the stage's bad-block entry (without that arrival a stage could be
+  // refilled before the softmax checks it).
+  constexpr uint32_t kMmaCount = 1;
 
   // ---------------------------------------------------------------- setup
   prefetch_schedule_inputs(a);
@@ -255,7 +224,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ms.tmem_base, 512);
     tmem_relinquish();
   }
-  if constexpr (PAIR) cluster_sync();   // both CTAs' barriers exist before any multicast
   pdl_wait();
   pdl_launch_dependents();
   prefill_setup(ms, a);
@@ -271,9 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1 both halves of V.
     const bool is_v = warp == 1;
     const bool primary = warp != 3;
-    // Paired form: each CTA loads its own 64-column half (rank) of every K
-    // and V tile into both CTAs, so a tile's boxes leave two SMs at once.
-    const int half_mask = (warp == 0 ? 1 : warp == 3 ? 2 : 3) & (PAIR ? 1 << rank : 3);
+    const int half_mask = warp == 0 ? 1 : warp == 3 ? 2 : 3;   // 64-column halves issued
     const int B = a.block_size;
     const int R = B < TT ? B : TT;            // rows per TMA box
     const int nbox = TT / R;                  // boxes per tile and 64-column half
@@ -294,11 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return raw;
     };
-    PfCursor<PAIR> cur;
+    PfCursor cur;
     cur.begin(a);
     UnitInfo ui;
-    // (A warp with no half to load and no barrier to arm has nothing to do.)
-    bool have = (half_mask != 0 || primary) && cur.step(ms, a, ui);
+    bool have = cur.step(ms, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -343,10 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = __shfl_sync(0xffffffffu, row, my_box);
       if (issuer) {
         uint8_t* dst = ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128;
-        if constexpr (PAIR)
-          tma_load_3d_mc(dst, map, &full[st], my_half * 64, ui.hk, r, 3);
-        else
-          tma_load_3d(dst, map, &full[st], my_half * 64, ui.hk, r);
+        tma_load_3d(dst, map, &full[st], my_half * 64, ui.hk, r);
       }
       ++jk;
       if (njl == 0) ++un;
@@ -388,11 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         kSwizzle128B);
           mma_f16_ts(d, tmem + b * 128 + k * 8, bd, id_o, !(pv_first && k == 0));
         }
-        if constexpr (PAIR) mma_commit_mc(&ms.v_empty[vs], 3); else mma_commit(&ms.v_empty[vs]);
+        mma_commit(&ms.v_empty[vs]);
         mma_commit(&ms.pv_done[b]);
         if (pv_last) mma_commit(&ms.o_full[ub]);
       };
-      PfCursor<PAIR> cur;
+      PfCursor cur;
       cur.begin(a);
       UnitInfo ui;
       while (ok && cur.step(ms, a, ui)) {
@@ -413,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(d, ad, bd, id_s, k > 0);
           }
           mma_commit(&ms.s_full[b]);
-          if constexpr (PAIR) mma_commit_mc(&ms.k_empty[ks], 3); else mma_commit(&ms.k_empty[ks]);
+          mma_commit(&ms.k_empty[ks]);
           if (jl == ui.ntiles - 1) mma_commit(&ms.q_empty[qb]);
           if (pv_j >= 0) issue_pv();
           pv_j = (int)j;
@@ -468,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pend = false;
       ++u_fin;
     };
-    PfCursor<PAIR> cur;
+    PfCursor cur;
     cur.begin(a);
     UnitInfo ui;
     while (ok && cur.step(ms, a, ui)) {
@@ -608,64 +570,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  // Paired form: no CTA leaves while its partner may still load into it.
-  if constexpr (PAIR) cluster_sync();
 }
 
 // Maximum dynamic shared memory, set once per device and kernel.
-template <bool BF16, bool PAIR>
+template <bool BF16>
 cudaError_t prepare() {
   static std::atomic<bool> attr_set[64];   // setting it twice from two threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<BF16, PAIR>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
-}
-
-void pair_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&attr)[2], int grid,
-                 cudaStream_t st) {
-  *cfg = {};
-  cfg->gridDim = dim3(grid);
-  cfg->blockDim = dim3(kThreads);
-  cfg->dynamicSmemBytes = kSmemBytes;
-  cfg->stream = st;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg->attrs = attr;
-  cfg->numAttrs = 2;
-}
-
-// Co-resident two-CTA clusters of the paired kernel, cached per device (0:
-// none, the single form is used).
-template <bool BF16>
-int pair_capacity() {
-  static std::atomic<int> cache[64];   // value + 1; 0 = not yet queried
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev].load(std::memory_order_relaxed) == 0) {
-    int n = 0;
-    if (prepare<BF16, true>() == cudaSuccess) {
-      cudaLaunchConfig_t cfg;
-      cudaLaunchAttribute attr[2];
-      pair_config(&cfg, attr, 2, nullptr);
-      if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<BF16, true>, &cfg) != cudaSuccess) {
-        cudaGetLastError();   // a refused query only means "no paired launch"
-        n = 0;
-      }
-    }
-    cache[dev].store(n + 1, std::memory_order_relaxed);
-  }
-  return cache[dev].load(std::memory_order_relaxed) - 1;
 }
 
 template <bool BF16>
@@ -681,25 +601,12 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // Paired form where chunks span several query tiles of at most 64 queries
-  // (g >= 2): the two tiles of a pair then need the same K/V tiles.
-  if (a.num_partitions >= 2 && g >= 2) {
-    const int cap = pair_capacity<BF16>();
-    const long long pairs = (long long)a.num_seqs * a.num_kv_heads * ((a.num_partitions + 1) / 2);
-    if (cap > 0) {
-      const int clusters = (int)(pairs < cap ? pairs : cap);
-      cudaLaunchConfig_t cfg;
-      cudaLaunchAttribute attr[2];
-      pair_config(&cfg, attr, 2 * clusters, st);
-      return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<BF16, true>, km, vm, qm, a);
-    }
-  }
-  cudaError_t e = prepare<BF16, false>();
+  cudaError_t e = prepare<BF16>();
   if (e != cudaSuccess) return e;
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   const int grid = (int)(units < sms ? units : sms);
-  return launch_pdl(prefill_tc_kernel<BF16, false>, dim3(grid), dim3(kThreads), kSmemBytes, st,
-                    km, vm, qm, a);
+  return launch_pdl(prefill_tc_kernel<BF16>, dim3(grid), dim3(kThreads), kSmemBytes, st, km, vm,
+                    qm, a);
 }
 
 }  // namespace

@@ -138,18 +138,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
-// Same, delivered to the same shared-memory offset (data and the
-// mbarrier's complete_tx) in every CTA of the cluster named by cta_mask.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const void* tmap, uint64_t* bar, int c0,
-                                               int c1, int c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Same as tma_load_3d, with an L2 eviction-priority hint (a createpolicy value).
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* tmap, uint64_t* bar,
                                                  int c0, int c1, int c2, uint64_t policy) {
@@ -305,16 +293,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// mma_commit arriving on the mbarrier at this shared-memory offset in every
-// CTA of the cluster named by cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 

@@ -126,9 +126,10 @@ def test_invalid_chunks_give_zero_rows_and_set_the_length_bit():
     assert_close_ulp(got, _oracle(c, max_query_len=35), "fp16", "chunk longer than max_query_len")
 
 
-def test_many_sequences_paired_form_reads_the_tables_from_global_memory():
-    # More than 1024 sequences with chunks of up to 3 query tiles (g = 8:
-    # 16 queries per tile): the paired form, its cursor on global memory.
+def test_many_sequences_with_multi_tile_chunks_read_the_tables_from_global_memory():
+    # More than 128 sequences (lengths and chunk bounds read from global
+    # memory, not the shared-memory table) with chunks of up to 3 query tiles
+    # (g = 8: 16 queries per tile).
     rng = np.random.default_rng(9)
     lens = rng.integers(1, 90, 1100)
     qlens = np.minimum(rng.integers(0, 48, 1100), lens)
@@ -138,7 +139,7 @@ def test_many_sequences_paired_form_reads_the_tables_from_global_memory():
     rows = [(int(r), int(h)) for r, h in zip(np.random.default_rng(10).integers(0, c.q.shape[0], 64),
                                              np.random.default_rng(11).integers(0, 16, 64))]
     ref = _oracle(c, rows=rows)
-    assert_close_ulp(np.stack([got[r, h] for r, h in rows]), ref, "bf16", "1100 sequences, paired")
+    assert_close_ulp(np.stack([got[r, h] for r, h in rows]), ref, "bf16", "1100 sequences, multi-tile chunks")
 
 
 def test_many_sequences_use_the_round_robin_schedule():

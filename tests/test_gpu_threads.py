@@ -1,10 +1,10 @@
 """Concurrent first calls from several host threads, in a fresh process.
 
 The launch code keeps per-device host state that the first call of each
-kernel sets: shared-memory size attributes, cluster and pair capacities,
-device attributes.  Seven threads make their first calls together, each on its
+kernel sets: shared-memory size attributes, cluster capacities, device
+attributes.  Seven threads make their first calls together, each on its
 own stream and each through a different kernel.  The kernels are CUDA-core
-decode, tensor-core decode, stream form, cluster form, paired prefill, and
+decode, tensor-core decode, stream form, cluster form, prefill, and
 bulk and 16-byte gathers.  Every output and status word must equal, bit for
 bit, the same call made afterwards with no other call running.
 """
