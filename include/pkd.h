@@ -123,6 +123,19 @@ PKD_API pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads
                            size_t* out_workspace_bytes);
 
 /*
+ * Workspace bytes that pkd_paged_decode_attention needs with partition_size
+ * 0 (the library's own plan) on the CURRENT device, for any num_kv_heads
+ * dividing num_heads and any supported block_size: the largest over those
+ * plans, so a buffer of this size serves every such call with these four
+ * sizes.  0 when no plan needs a workspace, and also when the sizes are
+ * invalid or the current device is not an sm_103 GPU (pkd_decode_plan
+ * reports those as errors, and gives the exact size for one configuration).
+ * Allocates nothing.
+ */
+PKD_API size_t pkd_decode_workspace_bytes(int num_seqs, int num_heads, int head_size,
+                                          int max_context_len);
+
+/*
  * Decode attention over a paged KV cache.
  *   out           [num_seqs][num_heads][head_size]            16-bit, written
  *   q             [num_seqs][num_heads][head_size]            16-bit

@@ -27,6 +27,7 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 _SIGS = {
     "pkd_decode_plan": (_c_int, [_c_int] * 7 + [ctypes.POINTER(_c_int)] * 3 +
                         [ctypes.POINTER(_c_size)]),
+    "pkd_decode_workspace_bytes": (_c_size, [_c_int] * 4),
     "pkd_paged_decode_attention": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
                                    [_c_float, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
     "pkd_paged_decode_attention_ex": (_c_int, [_vp] * 5 + [_c_int, _vp] + [_c_int] * 7 +
@@ -114,6 +115,12 @@ def decode_plan(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_co
                                ctypes.byref(npart), ctypes.byref(path), ctypes.byref(ws))
     _check("pkd_decode_plan", st)
     return ps.value, npart.value, path.value, ws.value
+
+
+def decode_workspace_bytes(num_seqs, num_heads, head_size, max_context_len):
+    """Workspace bytes that serve paged_decode_attention with partition_size 0
+    for any KV-head count and block size with these sizes (0: none needed)."""
+    return lib().pkd_decode_workspace_bytes(num_seqs, num_heads, head_size, max_context_len)
 
 
 def paged_decode_attention(out, q, key_cache, value_cache, block_tables, context_lens,

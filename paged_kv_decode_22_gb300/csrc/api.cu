@@ -21,6 +21,14 @@ pkd_status cuda_fail(cudaError_t e, const char* what) {
   return PKD_ERR_CUDA;
 }
 
+}  // namespace
+
+namespace pkd {
+pkd_status record_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+}  // namespace pkd
+
+namespace {
+
 struct DeviceInfo {
   int sms = 0;
   int major = 0;
@@ -216,6 +224,25 @@ pkd_status pkd_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int he
     *out_path = p.fused ? PKD_PATH_TC_CLUSTER : p.stream_ctas > 0 ? PKD_PATH_TC_STREAM : p.path;
   if (out_workspace_bytes) *out_workspace_bytes = p.ws_bytes;
   return PKD_OK;
+}
+
+size_t pkd_decode_workspace_bytes(int num_seqs, int num_heads, int head_size,
+                                  int max_context_len) {
+  // The largest workspace of the library's own plan (partition_size 0) over
+  // every KV-head count (a divisor of num_heads) and block size.
+  size_t worst = 0;
+  bool any = false;
+  for (int hk = 1; hk <= num_heads; ++hk) {
+    if (num_heads % hk) continue;
+    for (int bs = 8; bs <= 256; bs *= 2) {
+      Plan p;
+      if (make_plan(num_seqs, num_heads, hk, head_size, max_context_len, bs, 0, &p) != PKD_OK)
+        continue;
+      any = true;
+      worst = std::max(worst, p.ws_bytes);
+    }
+  }
+  return any ? worst : 0;
 }
 
 pkd_status pkd_paged_decode_attention(void* out, const void* q, const void* key_cache,

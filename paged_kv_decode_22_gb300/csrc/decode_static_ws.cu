@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "../../include/pkd.h"
+#include "internal.h"
 
 namespace {
 
@@ -36,15 +37,19 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_static_ws_addr[kMaxDevices];
 
-// Device address of g_static_ws on the current device (set up once per device).
+// Device address of g_static_ws on the current device (set up once per
+// device).  Called after the plan has checked the device.
 pkd_status static_ws_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKD_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return pkd::record_cuda_error(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return PKD_ERR_DEVICE;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (g_static_ws_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr) return PKD_ERR_CUDA;
+    e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess) return pkd::record_cuda_error(e, "cudaGetSymbolAddress(static workspace)");
+    if (p == nullptr) return pkd::record_cuda_error(cudaErrorInvalidSymbol, "cudaGetSymbolAddress(static workspace)");
     g_static_ws_addr[dev] = p;
   }
   *out = g_static_ws_addr[dev];
@@ -59,14 +64,19 @@ extern "C" PKD_API pkd_status pkd_paged_decode_attention_static_ws(
     int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_size,
     int block_size, int num_blocks, float scale, pkd_dtype dtype, int partition_size,
     uint32_t* device_status, void* stream) {
-  void* ws = nullptr;
-  pkd_status st = static_ws_address(&ws);
-  if (st != PKD_OK) return st;
+  // Arguments and the device first (the plan checks the device), then the
+  // scratch array's address.
+  if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
+    return PKD_ERR_NULL;
   size_t need = 0;
-  st = pkd_decode_plan(num_seqs, num_heads, num_kv_heads, head_size, block_size,
-                       max_context_len, partition_size, nullptr, nullptr, nullptr, &need);
+  pkd_status st = pkd_decode_plan(num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                                  max_context_len, partition_size, nullptr, nullptr, nullptr,
+                                  &need);
   if (st != PKD_OK) return st;
   if (need > (size_t)PKD_STATIC_WORKSPACE_BYTES) return PKD_ERR_WORKSPACE;
+  void* ws = nullptr;
+  st = static_ws_address(&ws);
+  if (st != PKD_OK) return st;
   return pkd_paged_decode_attention(out, q, key_cache, value_cache, block_tables,
                                     max_blocks_per_seq, context_lens, max_context_len, num_seqs,
                                     num_heads, num_kv_heads, head_size, block_size, num_blocks,

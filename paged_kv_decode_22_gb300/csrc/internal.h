@@ -7,7 +7,13 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/pkd.h"
+
 namespace pkd {
+
+// Records a failed CUDA call for pkd_last_error() on this host thread and
+// returns PKD_ERR_CUDA.
+pkd_status record_cuda_error(cudaError_t e, const char* what);
 
 // Launch with programmatic stream serialization (see pdl_wait in common.cuh).
 template <typename... KArgs, typename... Args>

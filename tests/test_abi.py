@@ -113,3 +113,13 @@ def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def test_workspace_bytes_is_zero_without_a_device_or_for_bad_sizes(lib):
+    # Pure host answer: no sm_103 device (or invalid sizes) means no plan.
+    import torch
+    assert lib.pkd_decode_workspace_bytes(4, 63, 128, 4096) == 0 or torch.cuda.is_available()
+    assert lib.pkd_decode_workspace_bytes(0, 64, 128, 4096) == 0
+    assert lib.pkd_decode_workspace_bytes(4, 64, 96, 4096) == 0
+    if not torch.cuda.is_available():
+        assert lib.pkd_decode_workspace_bytes(4, 64, 128, 4096) == 0

@@ -5,8 +5,9 @@ split-context scratch is an array built into the library.  This file is
 collected last so that a failure here cannot hide the other tests.  The test
 calls the entry point through the C ABI twice in a row, on different inputs,
 and checks each output against the ordinary entry point (caller-provided
-workspace) within the decode tolerance; it also checks that a plan needing
-more scratch than the built-in array is refused before any launch.
+workspace) and against the float64 oracle, within the decode tolerance; it
+also checks that a plan needing more scratch than the built-in array is
+refused before any launch.
 """
 import ctypes
 
@@ -15,10 +16,11 @@ import pytest
 import torch
 
 from oracle.formats import decode_bits
+from oracle.paged_attention import paged_decode_attention as attn_ref
 from paged_kv_decode_22_gb300 import _lib, ops
 from paged_kv_decode_22_gb300.workloads import make_decode_case
 
-from .gpu_util import ATOL_MAX, ATOL_MEAN, DeviceCase, down_bits
+from .gpu_util import ATOL_MAX, ATOL_MEAN, DeviceCase, assert_close, down_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -51,11 +53,13 @@ def test_static_scratch_entry_matches_ordinary_entry_twice(partition_size):
     cases = [_case(31, [4096, 777], 64, 8, "bf16"),
              _case(32, [3000, 129, 2048], 16, 16, "fp16") if partition_size >= 0
              else _case(34, [5000, 1, 0, 3333], 48, 1, "fp16")]
+    paths = []
     for dc in cases:                         # two calls in a row, different inputs
         c = dc.c
-        _, npart, _, ws_bytes = ops.decode_plan(c.num_seqs, c.num_heads, c.num_kv_heads, 128,
-                                                16, c.max_context_len, partition_size)
-        assert 0 < ws_bytes <= STATIC_BYTES or npart == 1
+        _, npart, path, ws_bytes = ops.decode_plan(c.num_seqs, c.num_heads, c.num_kv_heads, 128,
+                                                   16, c.max_context_len, partition_size)
+        assert ws_bytes <= STATIC_BYTES
+        paths.append((path, npart, ws_bytes))
         dt = torch.bfloat16 if c.dtype == "bf16" else torch.float16
         ref = torch.full(c.q.shape, float("nan"), dtype=dt, device="cuda")
         ops.paged_decode_attention(ref, dc.q, dc.kc, dc.vc, dc.bt, dc.cl, c.max_context_len,
@@ -70,6 +74,9 @@ def test_static_scratch_entry_matches_ordinary_entry_twice(partition_size):
         assert np.isfinite(got).all()
         err = np.abs(got - want)
         assert err.max() <= ATOL_MAX and err.mean() <= ATOL_MEAN, (err.max(), err.mean())
+        assert_close(got, attn_ref(c.q, c.key_cache, c.value_cache, c.block_tables,
+                                   c.context_lens, c.scale, c.dtype),
+                     f"static scratch, plan (path, partitions, scratch bytes) {paths[-1]}")
 
 
 def test_static_scratch_entry_refuses_plans_larger_than_its_array():
