@@ -1,17 +1,26 @@
 #!/usr/bin/env python3
-"""Benchmark: paged decode attention + gather_cached_kv on one GB300.
+"""Benchmark: paged decode attention on one GB300.
 
-One step is one pass of the whole hot path over one batch: a decode-attention
-call (split-context partitions + log-sum-exp merge when the plan splits) and a
-gather_cached_kv call.  Default workload: the LLaMA-13B-shaped MHA decode of
-"Optimizes the single_query_cached_kv_attention kernel" (8 sequences x 40
-heads, head_size 128, block_size 16, context 256, fp16, 2048-block pool) and
-the largest point of the gather sweep of "Memcpy kernel for flash attention"
-(2048 tokens, 40 heads, head_size 128, block_size 8, 1024 blocks, fp16).
+One step is one paged_decode_attention call on the long-context GQA decode of
+the kernel-latency table of "[Performance] Support MQA/GQA in decode phase by
+using FlashAttention" (context_len 4096, batch 256 row): 256 sequences, 64
+query heads on 8 KV heads, head_size 128, block_size 16, bf16, every
+sequence 4096 tokens through a seeded random block table over a 65536-block
+pool (4.3 GB of K and V).  The call covers address translation, query
+staging, both products, the online softmax, split-context partials and their
+log-sum-exp merge: the library plans the split, and at this size it takes
+the stream form (every SM an equal share of all tiles, cut pairs merged by a
+second launch).
 
 Prints ONE JSON line (rank 0).  `value` is algorithmic HBM bytes per step
-divided by device time per step (GB/s, 1e9).  Inputs rotate over enough
-device copies that every step reads data not left in L2 by the last one.
+(K and V of every cached token, q read, out written, block-table entries and
+lengths) divided by device time per step, GB/s (1e9).  The KV pool is 33x
+the L2, so every step streams its inputs from HBM.  Beside it: `e2e` (the
+same call with q, tables and lengths copied in from pinned host memory and
+out copied back, every step), `roofline` against the measured copy
+bandwidth, `cpu_baseline` (the float64 oracle on a sample of the same
+workload, one core and all cores), and side lines for the other decode
+workloads, gather_cached_kv and prefill.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkd|reference]
 """
@@ -30,34 +39,34 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
-# The CPU oracle legs run single-threaded; set before NumPy loads its BLAS.
+# The oracle runs one BLAS thread per process (the all-core leg uses one
+# process per core); set before NumPy loads its BLAS.
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 METRIC = ("paged decode attn µs/call and achieved HBM GB/s (% of GB300 roofline) "
           "vs oracle")
-WORKLOAD = "llama13b_mha_b8_ctx256 decode + gather_t2048"
-DECODE_CFG = "llama13b_mha_b8_ctx256"
-GATHER_CFG = "gather_t2048"
-# Decode workloads at batch >= 64 and context >= 1024, reported beside the
-# default line (decode alone).
-TARGETS = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "gqa_ctx4096_b256",
-           "mqa_ragged_b64"]
+HEADLINE = "gqa_ctx4096_b256"
+HEADLINE_DESC = "S=256 H=64 Hk=8 D=128 B=16 ctx=4096 NB=65536 bf16"
+# Side lines, decode alone: the other decode workloads at batch >= 64 and
+# context >= 1024, and the LLaMA-13B MHA decode.
+SIDE_DECODE = ["gqa_ctx1024_b64", "gqa_ctx1024_b256", "gqa_ctx4096_b64", "mqa_ragged_b64",
+               "llama13b_mha_b8_ctx256"]
+SIDE_GATHER = "gather_t2048"
 PATH_NAMES = {0: "simt", 1: "tc", 2: "tc_cluster", 3: "tc_stream"}   # decode_plan's kernel family
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-
-# DRAM traffic per launch of the dominant kernel from an ncu capture, keyed by
-# the sha256 (first 16 hex digits) of the kernel source it was taken on; the
-# value is reported only while that source is unchanged.
-NCU_TRAFFIC = {
-    # gather_t2048, profiles/gather_cached_kv_t2048.md: 41.97 MB read + 1.80 MB
-    # written during the kernel (its output is still dirty in L2 when it ends)
-    "aba4662af3507d10": 41969152 + 1797376,
-    # llama13b_mha_b8_ctx256, profiles/decode_simt_llama13b_mha_b8_ctx256.md
-    "90c0e845acbd2fec": 42051328 + 56576,
-}
+# ncu DRAM traffic per launch, stored with the hash of the sources it was
+# measured on; reported only while those sources are unchanged.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+DECODE_SOURCES = ("paged_kv_decode_22_gb300/csrc/decode_tc.cu",
+                  "paged_kv_decode_22_gb300/csrc/lse_reduce.cu",
+                  "paged_kv_decode_22_gb300/csrc/schedule.cuh",
+                  "paged_kv_decode_22_gb300/csrc/sm100.cuh",
+                  "paged_kv_decode_22_gb300/csrc/common.cuh",
+                  "paged_kv_decode_22_gb300/csrc/internal.h",
+                  "paged_kv_decode_22_gb300/csrc/api.cu")
 
 
 def max_over_ranks(ms, dist, device):
@@ -100,14 +109,6 @@ def decode_bytes(c) -> int:
 def gather_bytes(g) -> int:
     """K and V rows read and written once each, plus the slot mapping."""
     return 2 * 2 * g.num_tokens * g.num_heads * g.head_size * 2 + 8 * g.num_tokens
-
-
-def src_hash(*rel):
-    h = hashlib.sha256()
-    for r in rel:
-        with open(os.path.join(ROOT, r), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
 
 
 # ---------------------------------------------------------------- clocks
@@ -167,60 +168,166 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-# ---------------------------------------------------------------- reference arm (oracle)
+def src_hash(rel_paths):
+    h = hashlib.sha256()
+    for r in rel_paths:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
-def _oracle_sample(c, g, n):
-    """The first n units of the step: unit i = decode of (sequence i // H, head
-    i % H) over its whole context plus gather of 16 tokens."""
-    from oracle.gather import gather_cached_kv as ref_gather
+
+def stored_traffic(key, rel_paths):
+    """DRAM bytes per launch recorded for `key` in the traffic file, or None
+    when there is none or the sources changed since it was measured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sources_sha256_16") != src_hash(rel_paths):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def peaks():
+    """(HBM GB/s, its source, bf16 TF/s burst) from MEASURED_PEAKS.json."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, src, tf = FALLBACK_HBM_GBS, "fallback", FALLBACK_BF16_TFLOPS
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        if pk.get("hbm_gbs"):
+            hbm, src = float(pk["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+        if pk.get("bf16_tflops"):
+            tf = float(pk["bf16_tflops"])
+    return hbm, src, tf
+
+
+def timed_loop(call, steps, mark):
+    """The timed region: mark(0), exactly `steps` calls, mark(1)."""
+    mark(0)
+    for _ in range(steps):
+        call()
+    mark(1)
+
+
+def preroll_calls(call_us, window_s=0.6, cap=20000):
+    """Untimed calls that keep the GPU busy for about `window_s` before the
+    timed region, so that the clock samples see it under load."""
+    if not call_us or call_us <= 0:
+        return 0
+    return int(min(cap, math.ceil(window_s * 1e6 / call_us)))
+
+
+# ---------------------------------------------------------------- oracle (CPU baseline, reference arm)
+
+_ORACLE = {}
+
+
+def _oracle_sample_case(name, nseq):
+    """A sample of workload `name`: its first `nseq` sequences (lengths, head
+    shape, block size, dtype), on a pool of just the blocks they need."""
+    from paged_kv_decode_22_gb300.workloads import decode_configs, make_decode_case
+    cfg = dict(decode_configs()[name])
+    lens = [int(x) for x in cfg["context_lens"]][:nseq]
+    need = sum(-(-L // cfg["block_size"]) for L in lens)
+    cfg.update(num_seqs=len(lens), context_lens=lens, num_blocks=need, poison=False)
+    return make_decode_case(name=f"{name}[:{len(lens)}]", **cfg)
+
+
+def _oracle_init(name, nseq):
+    _ORACLE["case"] = _oracle_sample_case(name, nseq)
+
+
+def _oracle_pass(_=None):
+    """One oracle pass over the worker's sample: (seconds, bytes)."""
     from oracle.paged_attention import paged_decode_attention as ref_attn
-    H = c.num_heads
-    pairs = [(i // H, i % H) for i in range(n)]
-    tokens = g.slot_mapping[: min(g.num_tokens, 16 * n)]
-    per_pair = decode_bytes(c) / (c.num_seqs * H)
-    nbytes = per_pair * n + gather_bytes(g) * len(tokens) / g.num_tokens
+    c = _ORACLE["case"]
+    t0 = time.perf_counter()
+    ref_attn(c.q, c.key_cache, c.value_cache, c.block_tables, c.context_lens, c.scale, c.dtype)
+    return time.perf_counter() - t0, decode_bytes(c)
 
-    def run():
-        ref_attn(c.q, c.key_cache, c.value_cache, c.block_tables, c.context_lens, c.scale,
-                 c.dtype, pairs=pairs)
-        ref_gather(g.key_cache, g.value_cache, tokens)
-    return run, nbytes, f"decode (seq, head) pairs 0..{n - 1} of {c.num_seqs * H} + " \
-                        f"gather tokens 0..{len(tokens) - 1} of {g.num_tokens}"
+
+def _oracle_budget(budget_s):
+    """Oracle passes over the worker's sample until budget_s has elapsed:
+    (bytes processed, seconds, passes)."""
+    _oracle_pass()                       # first touch of the sample's pages
+    nbytes, n, t0 = 0, 0, time.perf_counter()
+    while True:
+        _, b = _oracle_pass()
+        nbytes += b
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return nbytes, el, n
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_pool(procs, name, nseq):
+    """`procs` spawned worker processes (one BLAS thread each), each holding
+    its own copy of the sample.  Spawned, so safe after CUDA is initialised."""
+    import multiprocessing as mp
+    return mp.get_context("spawn").Pool(procs, initializer=_oracle_init, initargs=(name, nseq))
+
+
+def cpu_baseline(name, budget_s=8.0, nseq=2):
+    """The oracle as it stands on this host's cores, on a bounded sample of
+    workload `name`: one process, then one process per core, each timing
+    passes over its own `nseq`-sequence sample for about budget_s."""
+    cores = host_cores()
+    _oracle_init(name, nseq)
+    b1, t1, n1 = _oracle_budget(budget_s)
+    one = round(b1 / t1 / 1e9, 4)
+    with oracle_pool(cores, name, nseq) as pool:
+        res = pool.map(_oracle_budget, [budget_s] * cores)
+    ball = sum(r[0] for r in res)
+    tall = max(r[1] for r in res)
+    allv = round(ball / tall / 1e9, 4)
+    what = (f"{name}: sequences 0..{nseq - 1} of the workload (same head shape, block size, "
+            f"context and dtype) per process, float64 oracle passes for ~{budget_s:.0f} s")
+    return {"value": allv, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{what}; {sum(r[2] for r in res)} passes over {cores} processes",
+            "single_core": {"value": one, "unit": "GB/s", "cores": 1, "passes": n1}}
 
 
 def run_reference(args, world, rank):
-    """The oracle as it stands, timed on the host cores, as the reference arm."""
+    """The oracle as it stands, timed on the host cores, as the reference arm:
+    each step is one oracle pass per core over a sample of the headline
+    workload, in parallel (one spawned process per core)."""
     if rank != 0:
         return 0
-    from paged_kv_decode_22_gb300.workloads import (decode_configs, gather_sweep,
-                                                    make_decode_case, make_gather_case)
-    c = make_decode_case(name=DECODE_CFG, **decode_configs()[DECODE_CFG])
-    g = make_gather_case(name=GATHER_CFG, **gather_sweep()[GATHER_CFG])
-    full = c.num_seqs * c.num_heads
-    # Size the per-step sample so that warm-up + timed steps take about 60 s.
-    run1, _, _ = _oracle_sample(c, g, 1)
-    t0 = time.perf_counter()
-    for _ in range(5):
-        run1()
-    t_unit = (time.perf_counter() - t0) / 5
-    n = int(max(1, min(full, 60.0 / max(1, args.steps + args.warmup) / t_unit)))
-    run, nbytes, what = _oracle_sample(c, g, n)
-    for _ in range(args.warmup):
-        run()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        run()
-    dt = (time.perf_counter() - t0) / args.steps
-    value = nbytes / dt / 1e9
+    cores = host_cores()
+    # Size each process's sample so that warm-up + timed steps take ~60 s.
+    _oracle_init(HEADLINE, 1)
+    _oracle_pass()
+    t_seq = min(_oracle_pass()[0] for _ in range(2))
+    nseq = int(max(1, min(16, 60.0 / max(1, args.steps + args.warmup) / t_seq)))
+    with oracle_pool(cores, HEADLINE, nseq) as pool:
+        pool.map(_oracle_pass, range(cores))          # every worker built and warm
+        for _ in range(args.warmup):
+            pool.map(_oracle_pass, range(cores))
+        nbytes, t0 = 0, time.perf_counter()
+        for _ in range(args.steps):
+            nbytes += sum(r[1] for r in pool.map(_oracle_pass, range(cores)))
+        dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / args.steps / dt / 1e9
+    what = (f"{HEADLINE}: per step, one float64 oracle pass over sequences 0..{nseq - 1} of the "
+            f"workload in each of {cores} processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) fp16 inputs, random non-overlapping block tables)",
-        "config": {"workload": WORKLOAD, "sample": what},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": what},
+        "data": "synthetic (seeded N(0,1) bf16 inputs, random non-overlapping block tables)",
+        "config": {"workload": HEADLINE, "shape": HEADLINE_DESC, "sample": what},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": what},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -229,20 +336,6 @@ def run_reference(args, world, rank):
 
 
 # ---------------------------------------------------------------- our arm
-
-def cpu_baseline(c, g, budget_s=10.0):
-    """The oracle as it stands on the host, on a bounded sample of the step."""
-    run, nbytes, what = _oracle_sample(c, g, 16)
-    n, t0 = 0, time.perf_counter()
-    while True:
-        run()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    return {"value": round(nbytes * n / el / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle", "sample": f"{what}; {n} passes in {el:.1f} s"}
-
 
 def graph_time(fns, calls=32, reps=5):
     """Mean device time per call (us) of the calls fns[i % len(fns)], replayed
@@ -500,13 +593,61 @@ def run_sweep(args, local):
     return 0
 
 
+
+def decode_launches(npart, path):
+    """Kernel launches of one decode call under its plan: the stream form and
+    a split workspace plan add a merge launch; the cluster form merges in
+    place."""
+    if path == 3 or (path in (0, 1) and npart > 1):
+        return 2
+    return 1
+
+
+def side_lines(dev, ops, peak):
+    """Graph-timed side lines: decode workloads, gather, prefill."""
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_22_gb300.workloads import gather_sweep, make_gather_case, prefill_configs
+    out = {"decode": {}, "gather": {}, "prefill": {}}
+    for name in SIDE_DECODE:
+        us, nbytes, (ps, npx, pathx, _), ncopy = time_decode_workload(name, dev, ops)
+        out["decode"][name] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                               "frac": round(nbytes / us / 1e3 / peak, 3),
+                               "path": PATH_NAMES[pathx], "partitions": npx, "copies": ncopy}
+    g = make_gather_case(name=SIDE_GATHER, **gather_sweep()[SIDE_GATHER])
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.float16).to(dev)
+    nb = gather_bytes(g)
+    ncopy = max(1, min(8, math.ceil(3 * L2_BYTES / nb)))
+    sets = []
+    for _ in range(ncopy):
+        ko = torch.empty((g.num_tokens, g.num_heads, g.head_size), dtype=torch.float16, device=dev)
+        sets.append((ko, torch.empty_like(ko), up(g.key_cache), up(g.value_cache),
+                     torch.from_numpy(g.slot_mapping).to(dev)))
+    us = graph_time([lambda t=t: ops.gather_cached_kv(*t) for t in sets])
+    out["gather"][SIDE_GATHER] = {"us_per_call": round(us, 2), "GBps": round(nb / us / 1e3, 1),
+                                  "frac": round(nb / us / 1e3 / peak, 3), "copies": ncopy,
+                                  "pages_GiBps_one_way": round(nb / 2 / us / 1e3 * 1e9 / 2 ** 30, 1)}
+    del sets
+    torch.cuda.empty_cache()
+    _, _, tpeak = peaks()
+    for name in prefill_configs():
+        us, flops, nbytes, pcopies = time_prefill_workload(name, dev, ops)
+        tf = flops / us / 1e6
+        out["prefill"][name] = {"us_per_call": round(us, 2), "TFLOPs": round(tf, 1),
+                                "frac_tensor": round(tf / tpeak, 3),
+                                "GBps": round(nbytes / us / 1e3, 1), "copies": pcopies}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
-    ap.add_argument("--no-targets", action="store_true", help="skip the large-batch GQA lines")
+    ap.add_argument("--no-targets", action="store_true", help="skip the side lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--sweep", action="store_true",
                     help="time every decode workload and gather point (one JSON line each)")
@@ -519,6 +660,7 @@ def main():
                          "warmup + steps times (no timing, no JSON line), e.g. under ncu")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.steps = max(args.steps, 1)
 
     world = env_int("WORLD_SIZE", 1)
     rank = env_int("RANK", 0)
@@ -530,12 +672,9 @@ def main():
         return run_profile(args, local)
     if args.sweep:
         return run_sweep(args, local)
-    import numpy as np
     import torch
 
     from paged_kv_decode_22_gb300 import ops
-    from paged_kv_decode_22_gb300.workloads import (decode_configs, gather_sweep,
-                                                    make_decode_case, make_gather_case)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -549,206 +688,112 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    c = make_decode_case(name=DECODE_CFG, **decode_configs()[DECODE_CFG])
-    g = make_gather_case(name=GATHER_CFG, **gather_sweep()[GATHER_CFG])
-    f16 = torch.float16
-
-    def upd(a, dt=None):
-        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
-                             else np.ascontiguousarray(a))
-        return (t.view(dt) if dt is not None else t).to(dev)
-
-    step_bytes = decode_bytes(c) + gather_bytes(g)
-    # Rotation: enough independent device copies of every input and output
-    # that consecutive steps never find their data in L2 (touched bytes x
-    # copies > 3 x L2).
-    ncopy = max(2, math.ceil(3 * L2_BYTES / step_bytes))
-    sets = []
-    for _ in range(ncopy):
-        sets.append(dict(q=upd(c.q, f16), kc=upd(c.key_cache, f16), vc=upd(c.value_cache, f16),
-                         bt=upd(c.block_tables), cl=upd(c.context_lens),
-                         gkc=upd(g.key_cache, f16), gvc=upd(g.value_cache, f16),
-                         slots=upd(g.slot_mapping),
-                         out=torch.empty(c.q.shape, dtype=f16, device=dev),
-                         ko=torch.empty((g.num_tokens, g.num_heads, g.head_size), dtype=f16,
-                                        device=dev),
-                         vo=torch.empty((g.num_tokens, g.num_heads, g.head_size), dtype=f16,
-                                        device=dev)))
-    S, H, D = c.q.shape
-    ps, npart, path, ws_bytes = ops.decode_plan(S, H, c.num_kv_heads, D, c.block_size,
-                                                c.max_context_len)
+    peak, peak_src, _ = peaks()
+    d = device_decode_inputs(HEADLINE, dev)
+    S, H, D = d["q"].shape
+    Hk, B = d["kc"].shape[2], d["kc"].shape[1]
+    step_bytes = d["bytes"]
+    ps, npart, path, ws_bytes = ops.decode_plan(S, H, Hk, D, B, d["max_ctx"])
     work = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def decode_call(i, st=None):
-        d = sets[i % ncopy]
+    def call():
         ops.paged_decode_attention(d["out"], d["q"], d["kc"], d["vc"], d["bt"], d["cl"],
-                                   c.max_context_len, c.scale, workspace=work, stream=st)
+                                   d["max_ctx"], d["scale"], workspace=work, stream=stream)
 
-    def gather_call(i, st=None):
-        d = sets[i % ncopy]
-        ops.gather_cached_kv(d["ko"], d["vo"], d["gkc"], d["gvc"], d["slots"], stream=st)
-
-    launches_per_step = 2 + (1 if npart > 1 else 0)
-    for i in range(args.warmup):
-        decode_call(i, stream)
-        gather_call(i, stream)
+    # Warm-up, timed loosely to size the clock pre-roll.
     barrier()
-
-    # The timed steps replay CUDA graphs of CHUNK decode calls followed by CHUNK
-    # gather calls (inputs rotating over the device copies), so host launch
-    # overhead stays out of the device time.  Events between the two graphs
-    # give each kernel's average duration inside the same timed region.
-    CHUNK = 64
-
-    def capture(fn, n):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            for i in range(n):
-                fn(i)
-        return gr
-
-    full, rest = divmod(args.steps, CHUNK)
-    graphs = [(capture(decode_call, CHUNK), capture(gather_call, CHUNK))] if full else []
-    tail = (capture(decode_call, rest), capture(gather_call, rest)) if rest else None
-    plan = [graphs[0]] * full + ([tail] if tail else [])
+    t0 = time.perf_counter()
+    for _ in range(args.warmup):
+        call()
+    barrier()
+    warm_us = (time.perf_counter() - t0) * 1e6 / args.warmup
+    preroll = preroll_calls(warm_us)
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_id = None
-    for gd, gg in plan[:2]:
-        gd.replay()
-        gg.replay()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(plan) + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with ClockSampler(gpu_id) as clocks:
+        for _ in range(preroll):        # untimed: GPU under load while clocks are sampled
+            call()
         barrier()
-        evs[0].record(stream)
-        for j, (gd, gg) in enumerate(plan):
-            gd.replay()
-            evs[2 * j + 1].record(stream)
-            gg.replay()
-            evs[2 * j + 2].record(stream)
+        timed_loop(call, args.steps, lambda i: ev[i].record(stream))
         barrier()
-    total_ms = evs[0].elapsed_time(evs[-1])
-    dec_ms = sum(evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(len(plan)))
-    gat_ms = sum(evs[2 * j + 1].elapsed_time(evs[2 * j + 2]) for j in range(len(plan)))
-    ms = total_ms / args.steps
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
     ms = max_over_ranks(ms, dist, dev)
-    dec_us = dec_ms * 1e3 / args.steps
-    gat_us = gat_ms * 1e3 / args.steps
-    del graphs, tail, plan
+    us = ms * 1e3
 
-    # End to end through the public API with host buffers: per step, copy the
-    # step's inputs (q, block tables, context lengths, slot mapping) from
-    # pinned host memory, run both calls, read every output back to pinned host
-    # memory.  The KV pools are resident state, as in serving.
-    hq = torch.from_numpy(c.q.view(np.int16)).view(f16).pin_memory()
-    hbt = torch.from_numpy(c.block_tables).pin_memory()
-    hcl = torch.from_numpy(c.context_lens).pin_memory()
-    hsl = torch.from_numpy(g.slot_mapping).pin_memory()
-    hout = torch.empty(sets[0]["out"].shape, dtype=f16).pin_memory()
-    hko = torch.empty(sets[0]["ko"].shape, dtype=f16).pin_memory()
-    hvo = torch.empty(sets[0]["vo"].shape, dtype=f16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hcl, hsl))
-    d2h = sum(t.numel() * t.element_size() for t in (hout, hko, hvo))
+    # End to end through the public API with host buffers: every step copies
+    # q, the block tables and the lengths in from pinned host memory, runs the
+    # call and copies out back to pinned host memory.  The KV pool is resident
+    # state, as in serving.
+    hq = d["q"].cpu().pin_memory()
+    hbt = d["bt"].cpu().pin_memory()
+    hcl = d["cl"].cpu().pin_memory()
+    hout = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hcl))
+    d2h = hout.numel() * hout.element_size()
 
-    def e2e_step(i):
-        d = sets[i % ncopy]
+    def e2e_step():
         d["q"].copy_(hq, non_blocking=True)
         d["bt"].copy_(hbt, non_blocking=True)
         d["cl"].copy_(hcl, non_blocking=True)
-        d["slots"].copy_(hsl, non_blocking=True)
-        decode_call(i, stream)
-        gather_call(i, stream)
+        call()
         hout.copy_(d["out"], non_blocking=True)
-        hko.copy_(d["ko"], non_blocking=True)
-        hvo.copy_(d["vo"], non_blocking=True)
         stream.synchronize()
 
-    e2e_steps = max(20, min(2000, args.steps // 10))
-    for i in range(5):
-        e2e_step(i)
+    for _ in range(3):
+        e2e_step()
     barrier()
     t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
+    timed_loop(e2e_step, args.steps, lambda i: None)
     barrier()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dist, dev)
+    del d, work
+    torch.cuda.empty_cache()
 
-    # Large-batch decode lines (decode alone): inputs from a seeded torch
-    # generator on the device (timing does not depend on the values), CUDA
-    # graph replays over rotated copies, as in the timed region above.
-    targets = {}
+    sides = None
     if not args.no_targets:
-        for name in TARGETS:
-            us, nbytes, (ps, npx, pathx, _), tcopies = time_decode_workload(name, dev, ops)
-            targets[name] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
-                             "path": PATH_NAMES[pathx], "partitions": npx,
-                             "copies": tcopies}
-
-    # Prefill lines (tensor-bound): same method, FLOPs against the bf16 peak.
-    prefill_lines = {}
-    if not args.no_targets:
-        from paged_kv_decode_22_gb300.workloads import prefill_configs
-        for name in prefill_configs():
-            us, flops, nbytes, pcopies = time_prefill_workload(name, dev, ops)
-            prefill_lines[name] = {"us_per_call": round(us, 2), "TFLOPs": round(flops / us / 1e6, 1),
-                                   "GBps": round(nbytes / us / 1e3, 1), "copies": pcopies}
-
-    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    peak, peak_src = FALLBACK_HBM_GBS, "fallback"
-    tpeak = FALLBACK_BF16_TFLOPS
-    if os.path.exists(peaks_path):
-        with open(peaks_path) as f:
-            pk = json.load(f)
-        if pk.get("hbm_gbs"):
-            peak, peak_src = float(pk["hbm_gbs"]), "measured"
-        if pk.get("bf16_tflops"):
-            tpeak = float(pk["bf16_tflops"])
-    for v in targets.values():
-        v["frac"] = round(v["GBps"] / peak, 3)
-    for v in prefill_lines.values():
-        v["frac_tensor"] = round(v["TFLOPs"] / tpeak, 3)
+        sides = side_lines(dev, ops, peak)
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return 0
 
-    dec_b, gat_b = decode_bytes(c), gather_bytes(g)
-    if dec_us >= gat_us:
-        dom, dom_bytes, dom_us, dom_src = "decode", dec_b, dec_us, ("paged_kv_decode_22_gb300/csrc/decode_simt.cu",)
-    else:
-        dom, dom_bytes, dom_us, dom_src = "gather_cached_kv", gat_b, gat_us, ("paged_kv_decode_22_gb300/csrc/copy_kv.cu",)
-    achieved = dom_bytes / dom_us / 1e3
-    traffic = NCU_TRAFFIC.get(src_hash(*dom_src))
-    value = whole_job_gbps(step_bytes, world, ms)
+    achieved = step_bytes / us / 1e3
+    traffic = stored_traffic(HEADLINE, DECODE_SOURCES)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
-        "data": "synthetic (seeded N(0,1) fp16, random non-overlapping block tables)",
-        "config": {"workload": WORKLOAD, "decode": "S=8 H=40 Hk=40 D=128 B=16 ctx=256 NB=2048",
-                   "gather": "T=2048 H=40 D=128 B=8 NB=1024",
-                   "l2": f"inputs rotate over {ncopy} device copies (>3x L2 touched per cycle)",
-                   "decode_partitions": npart, "decode_path": PATH_NAMES[path]},
-        "decode_us_per_call": round(dec_us, 2), "gather_us_per_call": round(gat_us, 2),
+        "metric": METRIC, "value": round(whole_job_gbps(step_bytes, world, ms), 1),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "us_per_call": round(us, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 from a torch generator, random "
+                "non-overlapping block tables)",
+        "config": {"workload": HEADLINE, "shape": HEADLINE_DESC,
+                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of K/V per call "
+                         "streamed through the 129 MB L2 (no flush needed)",
+                   "decode_path": PATH_NAMES[path], "decode_partitions": npart,
+                   "clock_preroll_calls": preroll},
         "step_bytes": step_bytes,
-        "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": round(achieved / peak, 3), "traffic": traffic,
-                     "algorithmic_bytes": dom_bytes},
-        "e2e": {"value": round(step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
+        "gpu_launches": decode_launches(npart, path) * args.steps,
+        "roofline": {"kernel": "paged_decode_attention call (decode_tc_kernel + "
+                               "stream_merge_kernel)" if path == 3 else
+                               f"paged_decode_attention call ({PATH_NAMES[path]})",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 3),
+                     "traffic": traffic, "algorithmic_bytes": step_bytes},
+        "e2e": {"value": round(whole_job_gbps(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
-        "targets_decode": targets,
-        "targets_prefill": prefill_lines,
     }
+    if sides is not None:
+        line["side"] = sides
     if world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(c, g)
+        line["cpu_baseline"] = cpu_baseline(HEADLINE)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
