@@ -8,3 +8,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
+
+
+def pytest_terminal_summary(terminalreporter):
+    gu = sys.modules.get("tests.gpu_util")
+    use = getattr(gu, "ULP_ALLOWANCE_USE", None) if gu else None
+    if use and use["compared"]:
+        terminalreporter.write_line(
+            f"prefill tolerance: {use['needed']} of {use['compared']} compared elements were "
+            f"above 1e-2 and passed through the one-ulp allowance")

@@ -13,7 +13,7 @@ from oracle.formats import decode_bits
 from oracle.paged_attention import paged_decode_attention as oracle_attention
 from paged_kv_decode_22_gb300.workloads import decode_configs, make_decode_case
 
-from .gpu_util import DeviceCase, assert_close, run_decode, sample_pairs, up
+from .gpu_util import DeviceCase, assert_close, run_decode, up
 
 pytestmark = pytest.mark.gpu
 
@@ -42,14 +42,19 @@ def test_workload_parity_full(name):
 
 
 @pytest.mark.parametrize("name", LARGE)
-def test_workload_parity_sampled(name):
+def test_workload_parity_full_size(name):
+    # Every (sequence, head) row at full size, in the launch configuration the
+    # bench times (the library's own plan): the stream form's cut pairs and
+    # their merges at every range edge are all compared.
+    from paged_kv_decode_22_gb300 import ops
     dc = _device_case(name)
+    c = dc.c
+    plan = ops.decode_plan(c.num_seqs, c.num_heads, c.num_kv_heads, c.head_size, c.block_size,
+                           c.max_context_len)
     got, status = run_decode(dc)
     assert status == 0
     assert np.isfinite(got).all()
-    pairs = sample_pairs(dc.c, 48)
-    ref = _oracle(dc.c, pairs)
-    assert_close(np.stack([got[s, h] for s, h in pairs]), ref, name)
+    assert_close(got, _oracle(c), f"{name}, plan {plan}")
 
 
 @pytest.mark.parametrize("partition_size", [64, 128, 192, 512, 4096])
@@ -169,6 +174,28 @@ def test_bad_block_and_bad_length_set_status_and_zero_rows():
             assert (got[s] == 0).all()
         for s in (1, 3):
             assert_close(got[s], ref[s], f"seq {s}")
+
+
+def test_workspace_bytes_covers_every_plan_of_its_sizes():
+    from paged_kv_decode_22_gb300 import ops
+    for S, H, D, ctx in [(1, 64, 128, 4096), (4, 64, 128, 1024), (64, 48, 128, 8192),
+                         (8, 40, 128, 256), (256, 64, 128, 4096), (2, 4, 64, 40)]:
+        w = ops.decode_workspace_bytes(S, H, D, ctx)
+        need = [ops.decode_plan(S, H, hk, D, b, ctx)[3] for hk in range(1, H + 1) if H % hk == 0
+                for b in (8, 16, 32, 64, 128, 256)]
+        assert w == max(need), (S, H, D, ctx)
+    # A call with a workspace of exactly that size.
+    c = _ragged(29, 64, 8, 128, 16, [4096, 1, 2000, 3333], "bf16")
+    dc = DeviceCase(c)
+    w = ops.decode_workspace_bytes(4, 64, 128, c.max_context_len)
+    assert w > 0
+    work = torch.empty(w, dtype=torch.uint8, device="cuda")
+    out = torch.empty(c.q.shape, dtype=torch.bfloat16, device="cuda")
+    ops.paged_decode_attention(out, dc.q, dc.kc, dc.vc, dc.bt, dc.cl, c.max_context_len, c.scale,
+                               workspace=work)
+    torch.cuda.synchronize()
+    from .gpu_util import down_bits
+    assert_close(decode_bits(down_bits(out), "bf16"), _oracle(c), "workspace_bytes-sized workspace")
 
 
 def test_workspace_too_small_is_rejected():

@@ -149,6 +149,23 @@ def test_invalid_chunks_give_zero_rows_and_empty_chunks_give_none():
     assert (out[2:] == 0).all()
 
 
+def test_chunks_longer_than_max_query_len_give_zero_rows_and_others_are_unchanged():
+    # Reading of the invalid-input rule: a chunk longer than the caller's
+    # max_query_len is invalid (all its rows zero); a chunk of exactly
+    # max_query_len is attended, and no other sequence is affected.
+    c = make_prefill_case(seed=13, num_seqs=3, num_heads=4, num_kv_heads=2, head_size=8,
+                          block_size=4, num_blocks=24, context_lens=[9, 6, 12],
+                          query_lens=[4, 5, 3], dtype="fp16")
+    full = _run(c)
+    out = _run(c, max_query_len=4)
+    assert np.abs(full[4:9]).max() > 0                     # the 5-query chunk, unlimited
+    assert (out[4:9] == 0).all()                           # ... and over the limit
+    np.testing.assert_array_equal(out[:4], full[:4])       # n == max_query_len: attended
+    np.testing.assert_array_equal(out[9:], full[9:])
+    out = _run(c, max_query_len=5)
+    np.testing.assert_array_equal(out, full)
+
+
 def test_a_bad_block_zeroes_only_the_queries_that_see_it():
     c = make_prefill_case(seed=12, num_seqs=1, num_heads=2, num_kv_heads=1, head_size=8,
                           block_size=4, num_blocks=16, context_lens=[20], query_lens=[10],
