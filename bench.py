@@ -384,9 +384,10 @@ def time_decode_workload(name, dev, ops, partition_size=0):
     return us, nbytes, plan, ncopy
 
 
-def device_decode_inputs(name, dev):
+def device_decode_inputs(name, dev, tight=False):
     """Device inputs of a decode workload from a seeded torch generator (for
-    timing and profiling: the kernels' speed does not depend on the values)."""
+    timing and profiling: the kernels' speed does not depend on the values).
+    tight: a pool of just the blocks the sequences use (small ncu captures)."""
     import torch
 
     from paged_kv_decode_22_gb300.workloads import decode_configs
@@ -397,7 +398,7 @@ def device_decode_inputs(name, dev):
                       cfg["block_size"])
     lens = torch.tensor(cfg["context_lens"], dtype=torch.int32)
     need = (lens + B - 1) // B
-    nb = max(cfg["num_blocks"], int(need.sum()))
+    nb = int(need.sum()) if tight else max(cfg["num_blocks"], int(need.sum()))
     dt = torch.float16 if cfg["dtype"] == "fp16" else torch.bfloat16
     kc = torch.randn((nb, B, Hk, D), generator=gen, device=dev, dtype=dt)
     vc = torch.randn((nb, B, Hk, D), generator=gen, device=dev, dtype=dt)
@@ -490,7 +491,7 @@ def run_profile(args, local):
     dev = torch.device("cuda", local)
     kind, name = args.profile.split(":", 1)
     if kind == "decode":
-        d = device_decode_inputs(name, dev)
+        d = device_decode_inputs(name, dev, tight=args.tight_pool)
         S, H, D = d["q"].shape
         _, npart, _, ws = ops.decode_plan(S, H, d["kc"].shape[2], D, d["kc"].shape[1],
                                           d["max_ctx"], args.partition_size)
@@ -654,6 +655,8 @@ def main():
     ap.add_argument("--partition-size", type=int, default=0,
                     help="--sweep/--profile decode lines: forced partition_size "
                          "(0 = the library's plan, -1 = the stream form)")
+    ap.add_argument("--tight-pool", action="store_true",
+                    help="--profile decode: a pool of just the blocks the sequences use")
     ap.add_argument("--profile", default=None, metavar="KIND:NAME",
                     help="profiling mode: run only 'decode:<workload>', 'prefill:<workload>' or "
                          "'gather:<workload>' "
