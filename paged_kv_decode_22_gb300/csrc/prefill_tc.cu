@@ -5,28 +5,37 @@
 // note that the KV-cache attention kernel serves prefill as well, with or
 // without a cached prefix; this is that generalisation, shaped for prefill.
 //
-// Work unit = (sequence, KV head, tile of QT = 128 / g chunk queries): its
-// 128 rows are the (query, head) pairs r = query * g + head, so all g heads
-// of a query share every K/V tile.  A persistent grid of one CTA per SM walks
-// the units, dealt round-robin; inside the CTA:
-//   warps 0, 3 K producers (half 0 and the unit's Q tile; half 1): TMA boxes of one block x
-//              64 columns into a ring of 32 KB stages, block ids one tile
-//              ahead, out-of-range blocks from an out-of-bounds row (zeros).
+// Query tile = QT = 128 / g chunk queries of one (sequence, KV head): its 128
+// rows are the (query, head) pairs r = query * g + head, so all g heads of a
+// query share every K/V tile.  Two kernels, both persistent (one CTA per
+// SM, units dealt round-robin, heaviest first), 8 warps:
+//   warps 0, 3 K producers (half 0 and the unit's Q tiles; half 1): TMA boxes
+//              of one block x 64 columns into a ring of 32 KB stages, block
+//              ids one tile ahead, out-of-range blocks from an
+//              out-of-bounds row (zeros).
 //   warp 1     V producer, same boxes into its own ring.
 //   warp 2     MMA issuer (one thread):
 //                S = Q K^T   M = 128 rows, N = 128 tokens, K = head_size,
 //                            A = Q (shared memory), B = K tile, into TMEM;
 //                O += P V    M = 128 rows, N = head_size, K = 128 tokens,
 //                            A = P (TMEM, written by the softmax), B = V tile.
-//   warps 4-7  softmax: thread = TMEM lane = one row.  Its 128 logits of a
-//              tile are in registers, so the row maximum and sum need no
+//   warps 4-7  softmax: thread = TMEM lane = one row.  The row's 128 logits
+//              of a tile are in registers, so its maximum and sum need no
 //              other thread.  p = 2^(x - m_ref) with a reference maximum
 //              m_ref that moves only when a logit passes it by more than 8
 //              (log2 units); then l and the row of O (in TMEM) are rescaled.
 //              P goes back into TMEM as 16-bit pairs over the first 64
-//              columns of the tile's S buffer, the A operand of P V.
-// TMEM: S double-buffered (2 x 128 columns), O double-buffered by unit
-// parity (2 x 128), 512 columns.
+//              columns of the tile's S.
+// Single kernel: a unit is one query tile; S double-buffered by tile parity
+// and O by unit parity (512 TMEM columns), so a unit's output is written
+// after the next unit's first P.
+// Paired kernel: a unit is TWO consecutive query tiles (slots A and B) of
+// one (sequence, KV head) and every K/V tile serves both, so a tile carries
+// twice the MMA work it costs in TMA boxes and a CTA switches units half as
+// often.  TMEM holds S_A, S_B, O_A, O_B; the MMA order per K/V tile is S_A
+// S_B | P_A V, next S_A | P_B V, next S_B, so that each slot's next S runs
+// while the softmax works on the other slot.  A unit whose second tile does
+// not exist (the last of an odd count) runs slot A only.
 #include <cuda.h>
 
 #include <atomic>
@@ -43,36 +52,68 @@ using namespace sm100;
 
 constexpr int TT = 128;                  // tokens per tile (= MMA N of S)
 constexpr int HD = 128;                  // head_size of this path
-constexpr int ROWS = 128;                // (query, head) rows per unit (= MMA M)
+constexpr int ROWS = 128;                // (query, head) rows per query tile (= MMA M)
 constexpr int TILE_BYTES = TT * HD * 2;  // one K or V tile, 32 KB
 constexpr int Q_BYTES = ROWS * HD * 2;   // one Q tile, 32 KB
-constexpr int NK = 2, NV = 2;            // ring stages
+constexpr int NV = 2;                    // V ring stages (K: Layout::NK)
 constexpr int kPfTable = 128;            // sequences whose lengths and chunk bounds sit in shared memory
 constexpr int kThreads = 256;            // 8 warps
 constexpr int kSoftmaxThreads = 128;
 constexpr int kNoBlock = -2147483647 - 1;
 constexpr float kHeadroom = 8.f;         // log2 units: p < 2^8 between rescales
+constexpr int kPairMinTokens = 1024;     // paired kernel from this many visible tokens per query
+// TMEM columns of slot x's S and O.
+__host__ __device__ constexpr uint32_t col_s(int x) { return x ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t col_o(int x) { return x ? 384u : 256u; }
 
-constexpr int off_q = 0;
-constexpr int off_k = off_q + 2 * Q_BYTES;
-constexpr int off_v = off_k + NK * TILE_BYTES;
-constexpr int off_misc = off_v + NV * TILE_BYTES;
+// Shared memory: two Q tiles (the single kernel's by unit parity, the
+// paired kernel's slots A and B), the K ring, the V ring, then the barriers.
+template <bool PAIR>
+struct Layout {
+  static constexpr int NK = PAIR ? 3 : 2;
+  static constexpr int off_q = 0;
+  static constexpr int off_k = off_q + 2 * Q_BYTES;
+  static constexpr int off_v = off_k + NK * TILE_BYTES;
+  static constexpr int off_misc = off_v + NV * TILE_BYTES;
+};
 
-struct Misc {
-  uint64_t k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
+// Lengths and chunk bounds, in shared memory when there are at most
+// kPfTable sequences.
+struct PfTab {
+  int L[kPfTable];        // context_lens
+  int qs[kPfTable + 1];   // query_start
+};
+
+constexpr int kMiscBytes = 1280;
+struct MiscPair {
+  uint64_t k_full[Layout<true>::NK], k_empty[Layout<true>::NK], v_full[NV], v_empty[NV];
+  // per slot (A, B)
+  uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2], o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int k_bad[Layout<true>::NK];      // per K stage: token offset of the tile's first bad block id, or -1
+  PfTab tab;
+};
+static_assert(sizeof(MiscPair) <= kMiscBytes, "misc area too small");
+
+struct MiscSingle {
+  uint64_t k_full[Layout<false>::NK], k_empty[Layout<false>::NK], v_full[NV], v_empty[NV];
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2], o_full[2], o_empty[2], drain;
   uint32_t tmem_base;
   int abort;
-  int k_bad[NK];      // per K stage: token offset of the tile's first bad block id, or -1
-  int tab_L[kPfTable];        // context_lens, with at most kPfTable sequences
-  int tab_qs[kPfTable + 1];   // query_start, likewise
+  int k_bad[Layout<false>::NK];      // per K stage: token offset of the tile's first bad block id, or -1
+  PfTab tab;
 };
-constexpr int kMiscBytes = 1280;
-static_assert(sizeof(Misc) <= kMiscBytes, "misc area too small");
-constexpr int kSmemBytes = off_misc + kMiscBytes + 1024;   // + alignment slack
-static_assert(kSmemBytes <= 232448, "above the shared memory of one CTA");
+static_assert(sizeof(MiscSingle) <= kMiscBytes, "misc area too small");
 
-__device__ __forceinline__ void set_abort(Misc& ms, uint32_t* status) {
+template <bool PAIR>
+constexpr int smem_bytes() { return Layout<PAIR>::off_misc + kMiscBytes + 1024; }   // + alignment slack
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448,
+              "above the shared memory of one CTA");
+
+template <class M>
+__device__ __forceinline__ void set_abort(M& ms, uint32_t* status) {
   ms.abort = 1;
   flag(status, PKD_DEV_TIMEOUT);
 }
@@ -97,18 +138,18 @@ __device__ __forceinline__ int prefill_parts(const DecodeArgs& a, int q0, int q1
 // range up to the last one's position; ntiles = 0 when the chunk has no
 // such tile.  Lengths and chunk bounds come from the shared-memory table
 // when it holds them.
-__device__ __forceinline__ UnitInfo unit_at(const Misc& ms, const DecodeArgs& a, int s, int hk,
+__device__ __forceinline__ UnitInfo unit_at(const PfTab& tab, const DecodeArgs& a, int s, int hk,
                                             int p) {
   UnitInfo ui;
   ui.s = s;
   ui.hk = hk;
   ui.p = p;
   ui.slot = -1;
-  const bool tab = a.num_seqs <= kPfTable;
-  ui.L = tab ? ms.tab_L[s] : a.context_lens[s];
+  const bool in_tab = a.num_seqs <= kPfTable;
+  ui.L = in_tab ? tab.L[s] : a.context_lens[s];
   ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
-  const int q0 = tab ? ms.tab_qs[s] : a.query_start[s];
-  const int q1 = tab ? ms.tab_qs[s + 1] : a.query_start[s + 1];
+  const int q0 = in_tab ? tab.qs[s] : a.query_start[s];
+  const int q1 = in_tab ? tab.qs[s + 1] : a.query_start[s + 1];
   if (p < prefill_parts(a, q0, q1, ui.L)) {
     const int n = q1 - q0, i0 = p * a.q_per_unit;
     ui.nq = min(a.q_per_unit, n - i0);
@@ -126,11 +167,11 @@ __device__ __forceinline__ UnitInfo unit_at(const Misc& ms, const DecodeArgs& a,
 // The table, and zero rows (with the length status bit) for chunks that
 // cannot be attended: an invalid length, or longer than the context.  Every
 // thread calls this; it ends with __syncthreads().
-__device__ __forceinline__ void prefill_setup(Misc& ms, const DecodeArgs& a) {
+__device__ __forceinline__ void prefill_setup(PfTab& tab, const DecodeArgs& a) {
   if (a.num_seqs <= kPfTable)
     for (int i = threadIdx.x; i <= a.num_seqs; i += kThreads) {
-      if (i < a.num_seqs) ms.tab_L[i] = a.context_lens[i];
-      ms.tab_qs[i] = a.query_start[i];
+      if (i < a.num_seqs) tab.L[i] = a.context_lens[i];
+      tab.qs[i] = a.query_start[i];
     }
   for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
     const int L = a.context_lens[sq];
@@ -150,7 +191,7 @@ __device__ __forceinline__ void prefill_setup(Misc& ms, const DecodeArgs& a) {
 // Units of one CTA: unit u of S * Hk * P, dealt round-robin (consecutive
 // query tiles of a causal chunk differ in cost; dealing spreads them), later
 // (heavier) tiles first.
-struct PfCursor {
+struct SingleCursor {
   long long next, end;
   int stride;
   __device__ __forceinline__ void begin(const DecodeArgs& a) {
@@ -158,14 +199,14 @@ struct PfCursor {
     stride = gridDim.x;
     end = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
   }
-  __device__ __forceinline__ bool step(const Misc& ms, const DecodeArgs& a, UnitInfo& ui) {
+  __device__ __forceinline__ bool step(const PfTab& tab, const DecodeArgs& a, UnitInfo& ui) {
     const int per = a.num_partitions;
     while (next < end) {
       const int v = (int)next;
       next += stride;
       const int pp = per - 1 - v % per, sh = v / per;
       const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
-      ui = unit_at(ms, a, s, hk, pp);
+      ui = unit_at(tab, a, s, hk, pp);
       if (ui.ntiles) return true;
     }
     return false;
@@ -174,16 +215,16 @@ struct PfCursor {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+    prefill_single_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  uint8_t* qbuf = sm + off_q;
-  uint8_t* kbuf = sm + off_k;
-  uint8_t* vbuf = sm + off_v;
-  Misc& ms = *reinterpret_cast<Misc*>(sm + off_misc);
+  uint8_t* qbuf = sm + Layout<false>::off_q;
+  uint8_t* kbuf = sm + Layout<false>::off_k;
+  uint8_t* vbuf = sm + Layout<false>::off_v;
+  MiscSingle& ms = *reinterpret_cast<MiscSingle*>(sm + Layout<false>::off_misc);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = a.num_heads / a.num_kv_heads;
@@ -195,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- setup
   prefetch_schedule_inputs(a);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NK; ++i) {
+    for (int i = 0; i < Layout<false>::NK; ++i) {
       mbar_init(&ms.k_full[i], 1);
       mbar_init(&ms.k_empty[i], kMmaCount + kSoftmaxThreads);
       ms.k_bad[i] = -1;
@@ -226,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   pdl_wait();
   pdl_launch_dependents();
-  prefill_setup(ms, a);
+  prefill_setup(ms.tab, a);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -246,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int oob_row = a.num_blocks * B;     // first row past the pool: zero fill
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     uint8_t* ring = is_v ? vbuf : kbuf;
-    const int nst = is_v ? NV : NK;
+    const int nst = is_v ? NV : Layout<false>::NK;
     uint64_t* full = is_v ? ms.v_full : ms.k_full;
     uint64_t* empty = is_v ? ms.v_empty : ms.k_empty;
     const bool issuer = lane < 2 * nbox && ((half_mask >> (lane / nbox)) & 1);
@@ -260,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return raw;
     };
-    PfCursor cur;
+    SingleCursor cur;
     cur.begin(a);
     UnitInfo ui;
-    bool have = cur.step(ms, a, ui);
+    bool have = cur.step(ms.tab, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -273,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool nhave = true;
       int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nhave = cur.step(ms, a, nui);
+        nhave = cur.step(ms.tab, a, nui);
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
@@ -354,15 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&ms.pv_done[b]);
         if (pv_last) mma_commit(&ms.o_full[ub]);
       };
-      PfCursor cur;
+      SingleCursor cur;
       cur.begin(a);
       UnitInfo ui;
-      while (ok && cur.step(ms, a, ui)) {
+      while (ok && cur.step(ms.tab, a, ui)) {
         const int qb = un & 1;
         ok = ok && mbar_wait(&ms.q_full[qb], (un >> 1) & 1);
         for (int jl = 0; jl < ui.ntiles && ok; ++jl, ++j) {
-          const int ks = j % NK, b = j & 1;
-          ok = mbar_wait(&ms.k_full[ks], (j / NK) & 1);
+          const int ks = j % Layout<false>::NK, b = j & 1;
+          ok = mbar_wait(&ms.k_full[ks], (j / Layout<false>::NK) & 1);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d = tmem + b * 128;
@@ -430,10 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       pend = false;
       ++u_fin;
     };
-    PfCursor cur;
+    SingleCursor cur;
     cur.begin(a);
     UnitInfo ui;
-    while (ok && cur.step(ms, a, ui)) {
+    while (ok && cur.step(ms.tab, a, ui)) {
       const int ub = u & 1;
       const bool valid_row = qi < ui.nq;
       const int pos = valid_row ? ui.pos0 + qi : -1;      // last visible token
@@ -442,10 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l = 0.f;
       int bad_from = 0x7fffffff;
       for (int jl = 0; jl < ui.ntiles; ++jl, ++j) {
-        const int b = j & 1, ks = j % NK;
+        const int b = j & 1, ks = j % Layout<false>::NK;
         const int ts = jl * TT;
         ok = ok && mbar_wait(&ms.s_full[b], (j >> 1) & 1);
-        ok = ok && mbar_wait(&ms.k_full[ks], (j / NK) & 1);
+        ok = ok && mbar_wait(&ms.k_full[ks], (j / Layout<false>::NK) & 1);
         if (!ok) break;
         tc_fence_after();
         {
@@ -572,22 +613,551 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Maximum dynamic shared memory, set once per device and kernel.
+// A unit: query tiles 2pp (slot A) and 2pp + 1 (slot B) of one (sequence,
+// KV head), walked over the K/V tiles up to the later tile's last query.
+struct PairUnit {
+  int s, hk, L, t1, ntiles;
+  bool hasB;
+  int qrow0[2], nq[2], pos0[2];   // per slot: first packed q row, queries, first position
+};
+
+// Units of one CTA: unit u of S * Hk * ceil(P / 2), dealt round-robin
+// (consecutive query tiles of a causal chunk differ in cost; dealing spreads
+// them), later (heavier) pairs first.
+struct PairCursor {
+  long long next, end;
+  int stride, per;
+  __device__ __forceinline__ void begin(const DecodeArgs& a) {
+    per = (a.num_partitions + 1) / 2;
+    next = blockIdx.x;
+    stride = gridDim.x;
+    end = (long long)a.num_seqs * a.num_kv_heads * per;
+  }
+  __device__ __forceinline__ bool step(const PfTab& tab, const DecodeArgs& a, PairUnit& pu) {
+    while (next < end) {
+      const int v = (int)next;
+      next += stride;
+      const int pp = per - 1 - v % per, sh = v / per;
+      const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
+      const UnitInfo ua = unit_at(tab, a, s, hk, 2 * pp);
+      if (ua.ntiles == 0) continue;   // no tile 2pp, so no tile 2pp + 1 either
+      const UnitInfo ub = unit_at(tab, a, s, hk, 2 * pp + 1);
+      pu.s = s;
+      pu.hk = hk;
+      pu.L = ua.L;
+      pu.hasB = ub.ntiles > 0;
+      pu.t1 = pu.hasB ? ub.t1 : ua.t1;
+      pu.ntiles = pu.hasB ? ub.ntiles : ua.ntiles;
+      pu.qrow0[0] = ua.qrow0;
+      pu.nq[0] = ua.nq;
+      pu.pos0[0] = ua.pos0;
+      pu.qrow0[1] = pu.hasB ? ub.qrow0 : 0;
+      pu.nq[1] = pu.hasB ? ub.nq : 0;
+      pu.pos0[1] = pu.hasB ? ub.pos0 : 0;
+      return true;
+    }
+    return false;
+  }
+};
+
 template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap,
+                      const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  uint8_t* qbuf = sm + Layout<true>::off_q;
+  uint8_t* kbuf = sm + Layout<true>::off_k;
+  uint8_t* vbuf = sm + Layout<true>::off_v;
+  MiscPair& ms = *reinterpret_cast<MiscPair*>(sm + Layout<true>::off_misc);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = a.num_heads / a.num_kv_heads;
+
+  // ---------------------------------------------------------------- setup
+  prefetch_schedule_inputs(a);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Layout<true>::NK; ++i) {
+      // Freed by the MMA (after the tile's last S) and by the softmax, which
+      // reads the stage's bad-block entry: without its arrival a stage could
+      // be refilled before the softmax has checked it.
+      mbar_init(&ms.k_full[i], 1);
+      mbar_init(&ms.k_empty[i], 1 + kSoftmaxThreads);
+      ms.k_bad[i] = -1;
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&ms.v_full[i], 1);
+      mbar_init(&ms.v_empty[i], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ms.q_full[x], 1);
+      mbar_init(&ms.q_empty[x], 1);
+      mbar_init(&ms.s_full[x], 1);
+      mbar_init(&ms.p_full[x], kSoftmaxThreads);
+      mbar_init(&ms.pv_done[x], 1);
+      mbar_init(&ms.o_full[x], 1);
+    }
+    mbar_init(&ms.drain, 1);
+    ms.abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&qmap);
+  }
+  if (warp == 2) {
+    tmem_alloc(&ms.tmem_base, 512);
+    tmem_relinquish();
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  prefill_setup(ms.tab, a);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+
+  if (warp == 0 || warp == 1 || warp == 3) {
+    // ============================================================ producers
+    // Warp 0 issues K's first 64-column half (and owns the stage's barrier
+    // bookkeeping and the Q loads), warp 3 K's second half in parallel, warp
+    // 1 both halves of V.
+    const bool is_v = warp == 1;
+    const bool primary = warp != 3;
+    const int half_mask = warp == 0 ? 1 : warp == 3 ? 2 : 3;   // 64-column halves issued
+    const int B = a.block_size;
+    const int R = B < TT ? B : TT;            // rows per TMA box
+    const int nbox = TT / R;                  // boxes per tile and 64-column half
+    const int oob_row = a.num_blocks * B;     // first row past the pool: zero fill
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    uint8_t* ring = is_v ? vbuf : kbuf;
+    const int nst = is_v ? NV : Layout<true>::NK;
+    uint64_t* full = is_v ? ms.v_full : ms.k_full;
+    uint64_t* empty = is_v ? ms.v_empty : ms.k_empty;
+    const bool issuer = lane < 2 * nbox && ((half_mask >> (lane / nbox)) & 1);
+    const int my_box = lane % nbox, my_half = lane / nbox;
+    auto load_raw = [&](const PairUnit& t, int tj) {
+      int raw = kNoBlock;
+      if (lane < nbox) {
+        const int ts = tj * TT;
+        const int tok0 = B <= TT ? ts + lane * B : ts;
+        if (tok0 < t.t1) raw = __ldg(a.block_tables + (size_t)t.s * a.max_blocks_per_seq + tok0 / B);
+      }
+      return raw;
+    };
+    PairCursor cur;
+    cur.begin(a);
+    PairUnit pu;
+    bool have = cur.step(ms.tab, a, pu);
+    int jl = 0;
+    int raw = have ? load_raw(pu, 0) : kNoBlock;
+    uint32_t jk = 0, un = 0, unb = 0;   // tiles, units, units with slot B
+    bool ok = true;
+    while (have) {
+      PairUnit npu = pu;
+      bool nhave = true;
+      int njl = jl + 1;
+      if (njl >= pu.ntiles) {
+        nhave = cur.step(ms.tab, a, npu);
+        njl = 0;
+      }
+      const int nraw = nhave ? load_raw(npu, njl) : kNoBlock;
+      if (!is_v && primary && jl == 0 && lane == 0) {
+        // The unit's query tiles: box {64, g, QT} (rows (query, head)) over
+        // q [T][H][D], two 64-column halves per slot.
+        const uint32_t qbytes = (uint32_t)(g * a.q_per_unit * 256);
+        ok = mbar_wait(&ms.q_empty[0], (un & 1) ^ 1);
+        if (ok) {
+          mbar_arrive_expect_tx(&ms.q_full[0], qbytes);
+          tma_load_3d(qbuf, &qmap, &ms.q_full[0], 0, pu.hk * g, pu.qrow0[0]);
+          tma_load_3d(qbuf + ROWS * 128, &qmap, &ms.q_full[0], 64, pu.hk * g, pu.qrow0[0]);
+        }
+        if (ok && pu.hasB) {
+          ok = mbar_wait(&ms.q_empty[1], (unb & 1) ^ 1);
+          if (ok) {
+            mbar_arrive_expect_tx(&ms.q_full[1], qbytes);
+            tma_load_3d(qbuf + Q_BYTES, &qmap, &ms.q_full[1], 0, pu.hk * g, pu.qrow0[1]);
+            tma_load_3d(qbuf + Q_BYTES + ROWS * 128, &qmap, &ms.q_full[1], 64, pu.hk * g,
+                        pu.qrow0[1]);
+          }
+        }
+      }
+      const int ts = jl * TT;
+      const bool bad = raw != kNoBlock && (raw < 0 || raw >= a.num_blocks);
+      const int row = (raw != kNoBlock && !bad) ? raw * B + (B <= TT ? 0 : ts % B) : oob_row;
+      const uint32_t bad_lanes = __ballot_sync(0xffffffffu, bad);   // lanes < nbox: boxes in token order
+      const int st = jk % nst;
+      if (lane == 0) {
+        ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
+        if (ok && primary) {
+          if (!is_v) {
+            ms.k_bad[st] = bad_lanes ? (__ffs(bad_lanes) - 1) * R : -1;
+            if (bad_lanes) flag(a.status, PKD_DEV_BAD_BLOCK);
+          }
+          mbar_arrive_expect_tx(&full[st], TILE_BYTES);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int r = __shfl_sync(0xffffffffu, row, my_box);
+      if (issuer) {
+        uint8_t* dst = ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128;
+        tma_load_3d(dst, map, &full[st], my_half * 64, pu.hk, r);
+      }
+      ++jk;
+      if (njl == 0) {
+        ++un;
+        if (pu.hasB) ++unb;
+      }
+      have = nhave;
+      pu = npu;
+      jl = njl;
+      raw = nraw;
+    }
+    if (!ok && lane == 0) {
+      set_abort(ms, a.status);
+      for (uint32_t j = (jk >= (uint32_t)nst ? jk - nst : 0); j < jk; ++j)
+        mbar_wait(&full[j % nst], (j / nst) & 1, 100000000ull);
+    }
+  } else if (warp == 2) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(ROWS, TT, BF16, false, false);
+      const uint32_t id_o = idesc_f16(ROWS, HD, BF16, false, true);
+      const uint32_t qaddr = smem_u32(qbuf), kaddr = smem_u32(kbuf), vaddr = smem_u32(vbuf);
+      uint32_t j = 0, jb = 0, un = 0, unb = 0;   // tiles (slot B's separately), units
+      bool ok = true;
+      // S_X(tile jj) = Q_X K^T into slot X's S columns.
+      auto issue_s = [&](int x, uint32_t jj) {
+        const int ks = jj % Layout<true>::NK;
+        const uint32_t d = tmem + col_s(x);
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t ad = smem_desc(qaddr + x * Q_BYTES + (k >> 2) * ROWS * 128 + (k & 3) * 32,
+                                        16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(kaddr + ks * TILE_BYTES + (k >> 2) * TT * 128 + (k & 3) * 32,
+                                        16, 1024, kSwizzle128B);
+          mma_f16(d, ad, bd, id_s, k > 0);
+        }
+        mma_commit(&ms.s_full[x]);
+      };
+      // O_X += P_X V (tile jj; `first`: the unit's first tile overwrites O_X).
+      auto issue_pv = [&](int x, uint32_t jj, bool first) {
+        const int vs = jj % NV;
+        const uint32_t d = tmem + col_o(x);
+#pragma unroll
+        for (int k = 0; k < TT / 16; ++k) {
+          const uint64_t bd = smem_desc(vaddr + vs * TILE_BYTES + k * 2048, TT * 128, 1024,
+                                        kSwizzle128B);
+          mma_f16_ts(d, tmem + col_s(x) + k * 8, bd, id_o, !(first && k == 0));
+        }
+        mma_commit(&ms.pv_done[x]);
+      };
+      PairCursor cur;
+      cur.begin(a);
+      PairUnit pu;
+      while (ok && cur.step(ms.tab, a, pu)) {
+        const int nt = pu.ntiles;
+        const bool hb = pu.hasB;
+        // The unit's first S of each slot.
+        ok = mbar_wait(&ms.q_full[0], un & 1);
+        if (ok && hb) ok = mbar_wait(&ms.q_full[1], unb & 1);
+        ok = ok && mbar_wait(&ms.k_full[j % Layout<true>::NK], (j / Layout<true>::NK) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(0, j);
+        if (hb) issue_s(1, j);
+        mma_commit(&ms.k_empty[j % Layout<true>::NK]);
+        if (nt == 1) {
+          mma_commit(&ms.q_empty[0]);
+          if (hb) mma_commit(&ms.q_empty[1]);
+        }
+        for (int jl = 0; jl < nt && ok; ++jl) {
+          const uint32_t jj = j + jl;
+          const bool more = jl + 1 < nt;
+          // Slot A: P_A V, then (the S_A columns free again) the next S_A.
+          ok = mbar_wait(&ms.v_full[jj % NV], (jj / NV) & 1) &&
+               mbar_wait(&ms.p_full[0], jj & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, jj, jl == 0);
+          if (jl == nt - 1) mma_commit(&ms.o_full[0]);
+          if (more) {
+            ok = mbar_wait(&ms.k_full[(jj + 1) % Layout<true>::NK], ((jj + 1) / Layout<true>::NK) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(0, jj + 1);
+          }
+          // Slot B likewise.
+          if (hb) {
+            ok = mbar_wait(&ms.p_full[1], (jb + jl) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(1, jj, jl == 0);
+            if (jl == nt - 1) mma_commit(&ms.o_full[1]);
+            if (more) issue_s(1, jj + 1);
+          }
+          mma_commit(&ms.v_empty[jj % NV]);
+          if (more) {
+            mma_commit(&ms.k_empty[(jj + 1) % Layout<true>::NK]);
+            if (jl + 2 == nt) {   // the unit's last S of each slot
+              mma_commit(&ms.q_empty[0]);
+              if (hb) mma_commit(&ms.q_empty[1]);
+            }
+          }
+        }
+        j += nt;
+        if (hb) jb += nt;
+        ++un;
+        if (hb) ++unb;
+      }
+      if (!ok) set_abort(ms, a.status);
+      mma_commit(&ms.drain);
+      mbar_wait(&ms.drain, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ============================================================ softmax / epilogue
+    const int wq = warp & 3;                   // TMEM lane quadrant
+    const int row = wq * 32 + lane;            // this thread's row of S, P and O (both slots)
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const float qscale = a.scale * kLog2e;
+    const int H = a.num_heads;
+    const int qi = row / g, hj = row - qi * g; // row = (tile query qi, head hj of the group)
+    const bool alibi = a.alibi != nullptr;
+    uint32_t j = 0, jb = 0, un = 0, unb = 0;
+    bool ok = true;
+    // Write slot x's row of a finished unit (output row `orow`, -1 for an
+    // invalid row): wait for its last P V, read O_x from TMEM, scale by
+    // `inv` and store 16-bit.
+    auto finalize = [&](int x, uint32_t phase, long long orow, float inv) {
+      ok = ok && mbar_wait(&ms.o_full[x], phase & 1);
+      if (!ok) return;
+      tc_fence_after();
+      const bool wr = orow >= 0;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (size_t)(wr ? orow : 0) * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld32(lane_addr + col_o(x) + c * 32, v);
+        if (wr) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[c * 4 + i] = make_uint4(pack2<BF16>(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                        pack2<BF16>(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                        pack2<BF16>(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                        pack2<BF16>(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+        }
+      }
+      tc_fence_before();
+    };
+    // Slot B of a finished unit is written after the next unit's first P_A
+    // (its last P V, issued after the unit's last P_B, completes meanwhile):
+    // the pending write's state.
+    bool pend = false;
+    uint32_t pend_phase = 0;
+    long long pend_row = -1;
+    float pend_inv = 0.f;
+    auto finish_pending = [&]() {
+      pend = false;
+      finalize(1, pend_phase, pend_row, pend_inv);
+    };
+    // Output row of this thread in slot x, -1 when it is not a valid row,
+    // and the factor 1 / l (0 when a bad block precedes the query).
+    auto out_row = [&](bool valid, int qrow0, int hk) {
+      return valid ? (long long)(qrow0 + qi) * H + hk * g + hj : -1ll;
+    };
+    auto inv_of = [&](bool valid, int pos, float lx, int bad_from) {
+      return !valid || pos >= bad_from || lx == 0.f ? 0.f : 1.f / lx;
+    };
+    PairCursor cur;
+    cur.begin(a);
+    PairUnit pu;
+    while (ok && cur.step(ms.tab, a, pu)) {
+      const bool hb = pu.hasB;
+      // Per slot (A, B): row validity, position (last visible token),
+      // reference maximum (+inf: p = 0, never rescales) and sum; the slope
+      // is the row's head's, the first bad token the unit's.
+      const bool valid_a = qi < pu.nq[0], valid_b = hb && qi < pu.nq[1];
+      const int pos_a = valid_a ? pu.pos0[0] + qi : -1, pos_b = valid_b ? pu.pos0[1] + qi : -1;
+      const float slope = alibi ? a.alibi[pu.hk * g + hj] * kLog2e : 0.f;
+      float m_a = valid_a ? -INFINITY : INFINITY, m_b = valid_b ? -INFINITY : INFINITY;
+      float l_a = 0.f, l_b = 0.f;
+      int bad_from = 0x7fffffff;
+      for (int jl = 0; jl < pu.ntiles && ok; ++jl, ++j) {
+        const int ks = j % Layout<true>::NK;
+        const int ts = jl * TT;
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {
+          if (x == 1 && !hb) break;
+          const uint32_t jx = x == 0 ? j : jb + jl;   // this slot's tile count (barrier phase)
+          const int p_x = x ? pos_b : pos_a;
+          float m_ref = x ? m_b : m_a, l_x = x ? l_b : l_a;
+          ok = ok && mbar_wait(&ms.s_full[x], jx & 1);
+          if (x == 0) {
+            ok = ok && mbar_wait(&ms.k_full[ks], (j / Layout<true>::NK) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const int kb = ms.k_bad[ks];
+            if (kb >= 0) bad_from = min(bad_from, ts + kb);
+            mbar_arrive(&ms.k_empty[ks]);
+          }
+          if (!ok) break;
+          tc_fence_after();
+          // This row's logits for the tile, log2 units, masked past the query.
+          float xv[TT];
+#pragma unroll
+          for (int c = 0; c < TT / 32; ++c) {
+            float v[32];
+            tmem_ld32(lane_addr + col_s(x) + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xv[c * 32 + i] = v[i];
+          }
+          // Without ALiBi the scale folds into the exponent's FMA (sc =
+          // scale * log2 e > 0: the maximum of x is the maximum of the
+          // logits); with ALiBi x carries the scale and the bias.
+          const bool fold = !alibi && qscale > 0.f;
+          const float sc = fold ? qscale : 1.f;
+          if (!fold) {
+#pragma unroll
+            for (int i = 0; i < TT; ++i) {
+              const int t = ts + i;
+              xv[i] = t <= p_x ? fmaf(xv[i], qscale, slope * (float)(t - p_x)) : -INFINITY;
+            }
+          } else if (ts + TT - 1 > p_x) {         // the tile passes this row's query
+#pragma unroll
+            for (int i = 0; i < TT; ++i) xv[i] = ts + i <= p_x ? xv[i] : -INFINITY;
+          }
+          // Row maximum: 8 independent chains, then a 3-level tree.
+          float m8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = xv[k];
+#pragma unroll
+          for (int i = 8; i < TT; i += 8)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], xv[i + k]);
+          const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sc;
+          float alpha = 1.f;
+          if (mx > m_ref + kHeadroom) {
+            const float m_new = fmaxf(m_ref, mx);
+            alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m_new);
+            l_x *= alpha;
+            m_ref = m_new;
+          }
+          // Rows whose reference moved rescale their O (accumulated in TMEM
+          // by the slot's previous P V) once that P V has completed.
+          if (__any_sync(0xffffffffu, alpha != 1.f && jl > 0)) {
+            ok = ok && mbar_wait(&ms.pv_done[x], (jx - 1) & 1);
+            tc_fence_after();
+            const uint32_t o_addr = lane_addr + col_o(x);
+#pragma unroll
+            for (int c = 0; c < HD / 16; ++c) {
+              float v[16];
+              uint32_t w[16];
+              tmem_ld16(o_addr + c * 16, v);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * alpha);
+              tmem_st16(o_addr + c * 16, w);
+            }
+            tmem_wait_st();
+          }
+          // P = 2^(x * sc - m_ref), 16-bit pairs over the slot's S columns
+          // 0..63, stored 16 columns at a time; the row sum in 4 chains.
+          float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = fast_exp2(fmaf(xv[c * 32 + 2 * i], sc, -m_ref));
+              const float p1 = fast_exp2(fmaf(xv[c * 32 + 2 * i + 1], sc, -m_ref));
+              l4[(2 * i) & 3] += p0;
+              l4[(2 * i + 1) & 3] += p1;
+              w[i] = pack2<BF16>(p0, p1);
+            }
+            tmem_st16(lane_addr + col_s(x) + c * 16, w);
+          }
+          l_x += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+          if (x) {
+            m_b = m_ref;
+            l_b = l_x;
+          } else {
+            m_a = m_ref;
+            l_a = l_x;
+          }
+          // Cache slots past the sequence end inside a loaded block may hold
+          // anything (NaN included): zero those V rows before either P V
+          // reads them (thread `row` clears token row `row` of the tile).
+          if (x == 0 && ts + TT > pu.L) {
+            const int vs = j % NV;
+            ok = ok && mbar_wait(&ms.v_full[vs], (j / NV) & 1);
+            if (ok && ts + row >= pu.L) {
+              uint4* v0 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + row * 128);
+              uint4* v1 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + TT * 128 + row * 128);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&ms.p_full[x]);
+          if (x == 0 && pend) finish_pending();
+        }
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- finish the unit
+      // Slot A now (its last P V ran during slot B's softmax), slot B after
+      // the next unit's first P_A.
+      finalize(0, un, out_row(valid_a, pu.qrow0[0], pu.hk), inv_of(valid_a, pos_a, l_a, bad_from));
+      if (hb) {
+        pend = true;
+        pend_phase = unb;
+        pend_row = out_row(valid_b, pu.qrow0[1], pu.hk);
+        pend_inv = inv_of(valid_b, pos_b, l_b, bad_from);
+        jb += pu.ntiles;
+        ++unb;
+      }
+      ++un;
+    }
+    if (ok && pend) finish_pending();
+    if (!ok && threadIdx.x == 128) set_abort(ms, a.status);
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Maximum dynamic shared memory, set once per device and kernel.
+template <bool BF16, bool PAIR>
 cudaError_t prepare() {
   static std::atomic<bool> attr_set[64];   // setting it twice from two threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = cudaFuncSetAttribute(PAIR ? prefill_pair_kernel<BF16> : prefill_single_kernel<BF16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<PAIR>());
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }
 
+// The paired kernel halves the K/V loads and the unit switches per query
+// tile but single-buffers Q, S and O, so each switch costs a pipeline
+// bubble: it pays when units are long.  It is taken for chunks of two or
+// more query tiles whose queries see at least kPairMinTokens cache tokens on
+// average by the host's bounds (a chunk over a long cached prefix): a
+// 256-token chunk after 3840 cached tokens ran 170.8 -> 161 us, 1024-token
+// prompts without prefix 237 -> 298 us.
 template <bool BF16>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   CUtensorMap km, vm, qm;
@@ -601,11 +1171,14 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = prepare<BF16>();
+  const bool pair = a.num_partitions >= 2 && a.max_context_len - a.max_query_len / 2 >= kPairMinTokens;
+  cudaError_t e = pair ? prepare<BF16, true>() : prepare<BF16, false>();
   if (e != cudaSuccess) return e;
-  const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+  const long long units =
+      (long long)a.num_seqs * a.num_kv_heads * (pair ? (a.num_partitions + 1) / 2 : a.num_partitions);
   const int grid = (int)(units < sms ? units : sms);
-  return launch_pdl(prefill_tc_kernel<BF16>, dim3(grid), dim3(kThreads), kSmemBytes, st, km, vm,
+  return launch_pdl(pair ? prefill_pair_kernel<BF16> : prefill_single_kernel<BF16>, dim3(grid),
+                    dim3(kThreads), pair ? smem_bytes<true>() : smem_bytes<false>(), st, km, vm,
                     qm, a);
 }
 

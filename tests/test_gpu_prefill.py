@@ -1,6 +1,12 @@
 """Prefill over the paged cache on the GPU (through the C ABI) against the
 float64 prefill oracle, outputs decoded from fp16/bf16.
 
+Two kernels serve prefill: the single form (one query tile per work unit)
+and the paired form (two query tiles of one sequence and KV head share every
+K/V tile), taken when the host's bounds promise long units.  Passing a large
+max_context_len (a valid upper bound) selects the paired form, so the tests
+run both on the same data.
+
 Tolerance: |err| <= 1e-2 + one ulp of the output type at |ref| (2^-7 |ref|
 for bf16, 2^-10 |ref| for fp16) per element, mean |err| <= 1e-3.  The ulp
 term is the final rounding itself: the first queries of a chunk without
@@ -36,8 +42,15 @@ def _case(seed, H, Hk, B, dtype, chunks, **kw):
                              query_lens=[n for _, n in chunks], dtype=dtype, **kw)
 
 
+# max_context_len that makes the host pick each form for the test chunks
+# (the paired form from max_context_len - max_query_len / 2 >= 1024).
+FORM_CTX = {"single": None, "pair": 8192}
+
+
 def _run(c, *, max_query_len=None, max_context_len=None, block_tables=None, context_lens=None,
-         alibi=None):
+         alibi=None, form="single"):
+    if max_context_len is None:
+        max_context_len = FORM_CTX[form]
     from paged_kv_decode_22_gb300 import ops
     b = c.base
     out = torch.full(c.q.shape, float("nan"), dtype=TORCH_DT[b.dtype], device="cuda")
@@ -60,20 +73,42 @@ def _oracle(c, **kw):
                           c.query_start, b.scale, b.dtype, **kw)
 
 
+@pytest.mark.parametrize("form", ["single", "pair"])
 @pytest.mark.parametrize("H,Hk,B,dtype", LAYOUTS)
-def test_prefill_matches_oracle(H, Hk, B, dtype):
+def test_prefill_matches_oracle(H, Hk, B, dtype, form):
     c = _case(61, H, Hk, B, dtype, CHUNKS)
-    got, status = _run(c)
+    got, status = _run(c, form=form)
     assert status == 0
-    assert_close_ulp(got, _oracle(c), dtype, f"prefill H{H}/{Hk} B{B} {dtype}")
+    assert_close_ulp(got, _oracle(c), dtype, f"prefill H{H}/{Hk} B{B} {dtype} {form}")
 
 
 @pytest.mark.parametrize("H,Hk,B,dtype", [(64, 8, 16, "bf16"), (32, 32, 16, "fp16"),
+                                          (64, 1, 32, "bf16"), (24, 8, 256, "fp16")])
+def test_paired_form_on_long_prefixes_with_its_own_bounds(H, Hk, B, dtype):
+    # Chunks over cached prefixes long enough that the host's own bounds pick
+    # the paired form; odd query-tile counts leave a unit with one slot.
+    chunks = [(4000, 300), (2500, 77), (1500, 1), (3100, 129), (2048, 0)]
+    c = _case(63, H, Hk, B, dtype, chunks)
+    assert c.base.max_context_len - 300 // 2 >= 1024
+    got, status = _run(c)
+    assert status == 0
+    assert_close_ulp(got, _oracle(c), dtype, f"paired, long prefixes H{H}/{Hk} B{B}")
+
+
+def test_both_forms_agree():
+    c = _case(65, 64, 8, 16, "bf16", CHUNKS)
+    a, _ = _run(c, form="single")
+    b, _ = _run(c, form="pair")
+    assert np.abs(a - b).max() <= 2e-2
+
+
+@pytest.mark.parametrize("form", ["single", "pair"])
+@pytest.mark.parametrize("H,Hk,B,dtype", [(64, 8, 16, "bf16"), (32, 32, 16, "fp16"),
                                           (48, 1, 16, "fp16")])
-def test_prefill_with_alibi(H, Hk, B, dtype):
+def test_prefill_with_alibi(H, Hk, B, dtype, form):
     c = _case(67, H, Hk, B, dtype, [(400, 150), (90, 90), (33, 1)])
     slopes = np.array([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], np.float32)
-    got, status = _run(c, alibi=slopes)
+    got, status = _run(c, alibi=slopes, form=form)
     assert status == 0
     assert_close_ulp(got, _oracle(c, alibi_slopes=slopes.astype(np.float64)), dtype,
                      "prefill alibi")
@@ -97,12 +132,13 @@ def test_one_query_per_sequence_equals_decode():
     assert_close_ulp(got, _oracle(c), "bf16", "one query per sequence")
 
 
-def test_bad_block_zeroes_only_the_queries_that_reach_it():
+@pytest.mark.parametrize("form", ["single", "pair"])
+def test_bad_block_zeroes_only_the_queries_that_reach_it(form):
     c = _case(73, 32, 4, 16, "bf16", [(400, 100), (200, 50)])
     good = _oracle(c)
     bt = c.base.block_tables.copy()
     bt[0, 20] = c.base.num_blocks + 5          # tokens 320..335: queries at positions >= 320
-    got, status = _run(c, block_tables=bt)
+    got, status = _run(c, block_tables=bt, form=form)
     assert status & 1
     c.base.block_tables = bt
     ref = _oracle(c)
@@ -126,7 +162,8 @@ def test_invalid_chunks_give_zero_rows_and_set_the_length_bit():
     assert_close_ulp(got, _oracle(c, max_query_len=35), "fp16", "chunk longer than max_query_len")
 
 
-def test_many_sequences_with_multi_tile_chunks_read_the_tables_from_global_memory():
+@pytest.mark.parametrize("form", ["single", "pair"])
+def test_many_sequences_with_multi_tile_chunks_read_the_tables_from_global_memory(form):
     # More than 128 sequences (lengths and chunk bounds read from global
     # memory, not the shared-memory table) with chunks of up to 3 query tiles
     # (g = 8: 16 queries per tile).
@@ -134,7 +171,7 @@ def test_many_sequences_with_multi_tile_chunks_read_the_tables_from_global_memor
     lens = rng.integers(1, 90, 1100)
     qlens = np.minimum(rng.integers(0, 48, 1100), lens)
     c = _case(87, 16, 2, 16, "bf16", [(int(L), int(n)) for L, n in zip(lens, qlens)])
-    got, status = _run(c)
+    got, status = _run(c, form=form)
     assert status == 0
     rows = [(int(r), int(h)) for r, h in zip(np.random.default_rng(10).integers(0, c.q.shape[0], 64),
                                              np.random.default_rng(11).integers(0, 16, 64))]
