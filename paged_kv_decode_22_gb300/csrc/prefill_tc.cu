@@ -34,8 +34,11 @@
 // twice the MMA work it costs in TMA boxes and a CTA switches units half as
 // often.  TMEM holds S_A, S_B, O_A, O_B; the MMA order per K/V tile is S_A
 // S_B | P_A V, next S_A | P_B V, next S_B, so that each slot's next S runs
-// while the softmax works on the other slot.  A unit whose second tile does
-// not exist (the last of an odd count) runs slot A only.
+// while the softmax works on the other slot.  Its softmax is two
+// warpgroups (12 warps in all): the two threads of a row each take 64 of its
+// 128 columns and agree on the row maximum through shared memory.  A unit
+// whose second tile does not exist (the last of an odd count) runs slot A
+// only.
 #include <cuda.h>
 
 #include <atomic>
@@ -57,7 +60,8 @@ constexpr int TILE_BYTES = TT * HD * 2;  // one K or V tile, 32 KB
 constexpr int Q_BYTES = ROWS * HD * 2;   // one Q tile, 32 KB
 constexpr int NV = 2;                    // V ring stages (K: Layout::NK)
 constexpr int kPfTable = 128;            // sequences whose lengths and chunk bounds sit in shared memory
-constexpr int kThreads = 256;            // 8 warps
+constexpr int kThreads = 256;            // single kernel: 8 warps
+constexpr int kThreadsPair = 384;        // paired kernel: 12 warps (two softmax warpgroups)
 constexpr int kSoftmaxThreads = 128;
 constexpr int kNoBlock = -2147483647 - 1;
 constexpr float kHeadroom = 8.f;         // log2 units: p < 2^8 between rescales
@@ -70,7 +74,7 @@ __host__ __device__ constexpr uint32_t col_o(int x) { return x ? 384u : 256u; }
 // paired kernel's slots A and B), the K ring, the V ring, then the barriers.
 template <bool PAIR>
 struct Layout {
-  static constexpr int NK = PAIR ? 3 : 2;
+  static constexpr int NK = 2;
   static constexpr int off_q = 0;
   static constexpr int off_k = off_q + 2 * Q_BYTES;
   static constexpr int off_v = off_k + NK * TILE_BYTES;
@@ -84,9 +88,12 @@ struct PfTab {
   int qs[kPfTable + 1];   // query_start
 };
 
-constexpr int kMiscBytes = 1280;
+constexpr int kMiscBytes = 1280;          // single kernel
+constexpr int kMiscBytesPair = 5376;      // paired kernel (+ the halves' maxima and sums)
 struct MiscPair {
   uint64_t k_full[Layout<true>::NK], k_empty[Layout<true>::NK], v_full[NV], v_empty[NV];
+  float xm[2][2][128];   // row maxima of the two column halves, [buffer][half][row]
+  float xl[2][2][128];   // row sums of the two column halves, [slot][half][row]
   // per slot (A, B)
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2], o_full[2];
   uint64_t drain;
@@ -95,7 +102,7 @@ struct MiscPair {
   int k_bad[Layout<true>::NK];      // per K stage: token offset of the tile's first bad block id, or -1
   PfTab tab;
 };
-static_assert(sizeof(MiscPair) <= kMiscBytes, "misc area too small");
+static_assert(sizeof(MiscPair) <= kMiscBytesPair, "misc area too small");
 
 struct MiscSingle {
   uint64_t k_full[Layout<false>::NK], k_empty[Layout<false>::NK], v_full[NV], v_empty[NV];
@@ -108,7 +115,9 @@ struct MiscSingle {
 static_assert(sizeof(MiscSingle) <= kMiscBytes, "misc area too small");
 
 template <bool PAIR>
-constexpr int smem_bytes() { return Layout<PAIR>::off_misc + kMiscBytes + 1024; }   // + alignment slack
+constexpr int smem_bytes() {
+  return Layout<PAIR>::off_misc + (PAIR ? kMiscBytesPair : kMiscBytes) + 1024;   // + alignment slack
+}
 static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448,
               "above the shared memory of one CTA");
 
@@ -168,8 +177,9 @@ __device__ __forceinline__ UnitInfo unit_at(const PfTab& tab, const DecodeArgs& 
 // cannot be attended: an invalid length, or longer than the context.  Every
 // thread calls this; it ends with __syncthreads().
 __device__ __forceinline__ void prefill_setup(PfTab& tab, const DecodeArgs& a) {
+  const int nthreads = blockDim.x;
   if (a.num_seqs <= kPfTable)
-    for (int i = threadIdx.x; i <= a.num_seqs; i += kThreads) {
+    for (int i = threadIdx.x; i <= a.num_seqs; i += nthreads) {
       if (i < a.num_seqs) tab.L[i] = a.context_lens[i];
       tab.qs[i] = a.query_start[i];
     }
@@ -182,7 +192,7 @@ __device__ __forceinline__ void prefill_setup(PfTab& tab, const DecodeArgs& a) {
       if (threadIdx.x == 0) flag(a.status, PKD_DEV_BAD_LEN);
       uint32_t* o = reinterpret_cast<uint32_t*>(a.out) + (size_t)q0 * a.num_heads * a.head_size / 2;
       const size_t words = (size_t)n * a.num_heads * a.head_size / 2;
-      for (size_t i = threadIdx.x; i < words; i += kThreads) o[i] = 0u;
+      for (size_t i = threadIdx.x; i < words; i += nthreads) o[i] = 0u;
     }
   }
   __syncthreads();
@@ -661,7 +671,7 @@ struct PairCursor {
 };
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsPair, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
@@ -684,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // reads the stage's bad-block entry: without its arrival a stage could
       // be refilled before the softmax has checked it.
       mbar_init(&ms.k_full[i], 1);
-      mbar_init(&ms.k_empty[i], 1 + kSoftmaxThreads);
+      mbar_init(&ms.k_empty[i], 1 + 2 * kSoftmaxThreads);
       ms.k_bad[i] = -1;
     }
     for (int i = 0; i < NV; ++i) {
@@ -695,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ms.q_full[x], 1);
       mbar_init(&ms.q_empty[x], 1);
       mbar_init(&ms.s_full[x], 1);
-      mbar_init(&ms.p_full[x], kSoftmaxThreads);
+      mbar_init(&ms.p_full[x], 2 * kSoftmaxThreads);
       mbar_init(&ms.pv_done[x], 1);
       mbar_init(&ms.o_full[x], 1);
     }
@@ -919,8 +929,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ============================================================ softmax / epilogue
+    // Two warpgroups: warp 4 + q and warp 8 + q share TMEM lanes 32q..32q+31
+    // (rows); warpgroup h takes columns [64h, 64h + 64) of S (tokens) and of
+    // O (head dims).  The two threads of a row agree on its maximum through
+    // shared memory and one 64-thread named barrier per tile; every barrier
+    // also ANDs their `ok`, so the two stop together.
     const int wq = warp & 3;                   // TMEM lane quadrant
+    const int hh = (warp - 4) >> 2;            // column half
     const int row = wq * 32 + lane;            // this thread's row of S, P and O (both slots)
+    const uint32_t bar = 1 + wq;               // named barrier of this row quadrant's two warps
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float qscale = a.scale * kLog2e;
     const int H = a.num_heads;
@@ -928,19 +945,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool alibi = a.alibi != nullptr;
     uint32_t j = 0, jb = 0, un = 0, unb = 0;
     bool ok = true;
-    // Write slot x's row of a finished unit (output row `orow`, -1 for an
-    // invalid row): wait for its last P V, read O_x from TMEM, scale by
-    // `inv` and store 16-bit.
+    // Write this thread's half of slot x's row of a finished unit (output
+    // row `orow`, -1 for an invalid row): wait for the slot's last P V, read
+    // O_x from TMEM, scale by `inv`, store 16-bit.
     auto finalize = [&](int x, uint32_t phase, long long orow, float inv) {
       ok = ok && mbar_wait(&ms.o_full[x], phase & 1);
       if (!ok) return;
       tc_fence_after();
       const bool wr = orow >= 0;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (size_t)(wr ? orow : 0) * HD);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (size_t)(wr ? orow : 0) * HD +
+                                            hh * 64);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
-        tmem_ld32(lane_addr + col_o(x) + c * 32, v);
+        tmem_ld32(lane_addr + col_o(x) + hh * 64 + c * 32, v);
         if (wr) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -953,18 +971,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
     };
     // Slot B of a finished unit is written after the next unit's first P_A
-    // (its last P V, issued after the unit's last P_B, completes meanwhile):
-    // the pending write's state.
+    // (its last P V, issued after the unit's last P_B, completes meanwhile).
     bool pend = false;
     uint32_t pend_phase = 0;
     long long pend_row = -1;
     float pend_inv = 0.f;
-    auto finish_pending = [&]() {
-      pend = false;
-      finalize(1, pend_phase, pend_row, pend_inv);
-    };
-    // Output row of this thread in slot x, -1 when it is not a valid row,
-    // and the factor 1 / l (0 when a bad block precedes the query).
     auto out_row = [&](bool valid, int qrow0, int hk) {
       return valid ? (long long)(qrow0 + qi) * H + hk * g + hj : -1ll;
     };
@@ -977,17 +988,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && cur.step(ms.tab, a, pu)) {
       const bool hb = pu.hasB;
       // Per slot (A, B): row validity, position (last visible token),
-      // reference maximum (+inf: p = 0, never rescales) and sum; the slope
-      // is the row's head's, the first bad token the unit's.
+      // reference maximum (+inf: p = 0, never rescales) and this half's sum;
+      // the slope is the row's head's, the first bad token the unit's.
       const bool valid_a = qi < pu.nq[0], valid_b = hb && qi < pu.nq[1];
       const int pos_a = valid_a ? pu.pos0[0] + qi : -1, pos_b = valid_b ? pu.pos0[1] + qi : -1;
       const float slope = alibi ? a.alibi[pu.hk * g + hj] * kLog2e : 0.f;
       float m_a = valid_a ? -INFINITY : INFINITY, m_b = valid_b ? -INFINITY : INFINITY;
       float l_a = 0.f, l_b = 0.f;
       int bad_from = 0x7fffffff;
-      for (int jl = 0; jl < pu.ntiles && ok; ++jl, ++j) {
+      for (int jl = 0; jl < pu.ntiles; ++jl, ++j) {
         const int ks = j % Layout<true>::NK;
         const int ts = jl * TT;
+        const int tc0 = ts + hh * 64;          // first token of this thread's columns
 #pragma unroll 1
         for (int x = 0; x < 2; ++x) {
           if (x == 1 && !hb) break;
@@ -997,43 +1009,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = ok && mbar_wait(&ms.s_full[x], jx & 1);
           if (x == 0) {
             ok = ok && mbar_wait(&ms.k_full[ks], (j / Layout<true>::NK) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            const int kb = ms.k_bad[ks];
-            if (kb >= 0) bad_from = min(bad_from, ts + kb);
+            if (ok) {
+              tc_fence_after();
+              const int kb = ms.k_bad[ks];
+              if (kb >= 0) bad_from = min(bad_from, ts + kb);
+            }
             mbar_arrive(&ms.k_empty[ks]);
           }
-          if (!ok) break;
           tc_fence_after();
-          // This row's logits for the tile, log2 units, masked past the query.
-          float xv[TT];
-          tmem_ld128(lane_addr + col_s(x), xv);   // one round trip (a 5 % gain here; the
-                                                   // single kernel runs faster with four)
-          // Without ALiBi the scale folds into the exponent's FMA (sc =
-          // scale * log2 e > 0: the maximum of x is the maximum of the
-          // logits); with ALiBi x carries the scale and the bias.
+          // This half row's logits for the tile, log2 units, masked past the query.
+          float xv[64];
           const bool fold = !alibi && qscale > 0.f;
           const float sc = fold ? qscale : 1.f;
-          if (!fold) {
+          float mpart = -INFINITY;
+          if (ok) {
+            tmem_ld64(lane_addr + col_s(x) + hh * 64, xv);
+            // Without ALiBi the scale folds into the exponent's FMA (sc =
+            // scale * log2 e > 0: the maximum of x is the maximum of the
+            // logits); with ALiBi x carries the scale and the bias.
+            if (!fold) {
 #pragma unroll
-            for (int i = 0; i < TT; ++i) {
-              const int t = ts + i;
-              xv[i] = t <= p_x ? fmaf(xv[i], qscale, slope * (float)(t - p_x)) : -INFINITY;
+              for (int i = 0; i < 64; ++i) {
+                const int t = tc0 + i;
+                xv[i] = t <= p_x ? fmaf(xv[i], qscale, slope * (float)(t - p_x)) : -INFINITY;
+              }
+            } else if (tc0 + 63 > p_x) {         // the half passes this row's query
+#pragma unroll
+              for (int i = 0; i < 64; ++i) xv[i] = tc0 + i <= p_x ? xv[i] : -INFINITY;
             }
-          } else if (ts + TT - 1 > p_x) {         // the tile passes this row's query
+            float m4[4];
 #pragma unroll
-            for (int i = 0; i < TT; ++i) xv[i] = ts + i <= p_x ? xv[i] : -INFINITY;
+            for (int k = 0; k < 4; ++k) m4[k] = xv[k];
+#pragma unroll
+            for (int i = 4; i < 64; i += 4)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], xv[i + k]);
+            mpart = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           }
-          // Row maximum: 8 independent chains, then a 3-level tree.
-          float m8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = xv[k];
-#pragma unroll
-          for (int i = 8; i < TT; i += 8)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], xv[i + k]);
-          const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sc;
+          // The row maximum: this half's and the other's.
+          const int xb = hb ? x : (jl & 1);
+          ms.xm[xb][hh][row] = mpart;
+          ok = named_barrier_and(bar, 64, ok);
+          if (!ok) break;
+          const float mx = fmaxf(mpart, ms.xm[xb][hh ^ 1][row]) * sc;
           float alpha = 1.f;
           if (mx > m_ref + kHeadroom) {
             const float m_new = fmaxf(m_ref, mx);
@@ -1042,13 +1060,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_ref = m_new;
           }
           // Rows whose reference moved rescale their O (accumulated in TMEM
-          // by the slot's previous P V) once that P V has completed.
+          // by the slot's previous P V) once that P V has completed; each
+          // thread its half of the row.
           if (__any_sync(0xffffffffu, alpha != 1.f && jl > 0)) {
             ok = ok && mbar_wait(&ms.pv_done[x], (jx - 1) & 1);
             tc_fence_after();
-            const uint32_t o_addr = lane_addr + col_o(x);
+            const uint32_t o_addr = lane_addr + col_o(x) + hh * 64;
 #pragma unroll
-            for (int c = 0; c < HD / 16; ++c) {
+            for (int c = 0; c < 4; ++c) {
               float v[16];
               uint32_t w[16];
               tmem_ld16(o_addr + c * 16, v);
@@ -1058,23 +1077,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
           }
-          // P = 2^(x * sc - m_ref), 16-bit pairs over the slot's S columns
-          // 0..63, stored 16 columns at a time; the row sum in 4 chains.
-          float l4[4] = {0.f, 0.f, 0.f, 0.f};
+          // P = 2^(x * sc - m_ref) for this half's 64 tokens: 16-bit pairs in
+          // S columns [32h, 32h + 32); the half's sum in 4 chains.
+          {
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t w[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float p0 = fast_exp2(fmaf(xv[c * 32 + 2 * i], sc, -m_ref));
-              const float p1 = fast_exp2(fmaf(xv[c * 32 + 2 * i + 1], sc, -m_ref));
+            for (int i = 0; i < 32; ++i) {
+              const float p0 = fast_exp2(fmaf(xv[2 * i], sc, -m_ref));
+              const float p1 = fast_exp2(fmaf(xv[2 * i + 1], sc, -m_ref));
               l4[(2 * i) & 3] += p0;
               l4[(2 * i + 1) & 3] += p1;
               w[i] = pack2<BF16>(p0, p1);
             }
-            tmem_st16(lane_addr + col_s(x) + c * 16, w);
+            tmem_st32(lane_addr + col_s(x) + hh * 32, w);
+            l_x += (l4[0] + l4[1]) + (l4[2] + l4[3]);
           }
-          l_x += (l4[0] + l4[1]) + (l4[2] + l4[3]);
           if (x) {
             m_b = m_ref;
             l_b = l_x;
@@ -1084,40 +1102,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // Cache slots past the sequence end inside a loaded block may hold
           // anything (NaN included): zero those V rows before either P V
-          // reads them (thread `row` clears token row `row` of the tile).
+          // reads them (this thread clears its half of token row `row`).
           if (x == 0 && ts + TT > pu.L) {
             const int vs = j % NV;
             ok = ok && mbar_wait(&ms.v_full[vs], (j / NV) & 1);
             if (ok && ts + row >= pu.L) {
-              uint4* v0 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + row * 128);
-              uint4* v1 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + TT * 128 + row * 128);
+              uint4* v0 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + hh * TT * 128 + row * 128);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
+              for (int i = 0; i < 8; ++i) v0[i] = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
           }
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&ms.p_full[x]);
-          if (x == 0 && pend) finish_pending();
+          if (x == 0 && pend) {
+            // The previous unit's slot B: its sums were exchanged at that
+            // unit's end.
+            pend = false;
+            finalize(1, pend_phase, pend_row, pend_inv);
+          }
         }
+        if (!ok) break;
       }
-      if (!ok) break;
       // ---------------------------------------------------------- finish the unit
-      // Slot A now (its last P V ran during slot B's softmax), slot B after
-      // the next unit's first P_A.
-      finalize(0, un, out_row(valid_a, pu.qrow0[0], pu.hk), inv_of(valid_a, pos_a, l_a, bad_from));
+      // Exchange the halves' sums; slot A now (its last P V ran during slot
+      // B's softmax), slot B after the next unit's first P_A.
+      ms.xl[0][hh][row] = l_a;
+      if (hb) ms.xl[1][hh][row] = l_b;
+      ok = named_barrier_and(bar, 64, ok);
+      if (!ok) break;
+      finalize(0, un, out_row(valid_a, pu.qrow0[0], pu.hk),
+               inv_of(valid_a, pos_a, l_a + ms.xl[0][hh ^ 1][row], bad_from));
       if (hb) {
         pend = true;
         pend_phase = unb;
         pend_row = out_row(valid_b, pu.qrow0[1], pu.hk);
-        pend_inv = inv_of(valid_b, pos_b, l_b, bad_from);
+        pend_inv = inv_of(valid_b, pos_b, l_b + ms.xl[1][hh ^ 1][row], bad_from);
         jb += pu.ntiles;
         ++unb;
       }
       ++un;
+      ok = named_barrier_and(bar, 64, ok);   // both threads go on together
     }
-    if (ok && pend) finish_pending();
+    if (ok && pend) finalize(1, pend_phase, pend_row, pend_inv);
     if (!ok && threadIdx.x == 128) set_abort(ms, a.status);
   }
 
@@ -1151,8 +1179,9 @@ cudaError_t prepare() {
 // bubble: it pays when units are long.  It is taken for chunks of two or
 // more query tiles whose queries see at least kPairMinTokens cache tokens on
 // average by the host's bounds (a chunk over a long cached prefix): a
-// 256-token chunk after 3840 cached tokens ran 170.8 -> 161 us, 1024-token
-// prompts without prefix 237 -> 298 us.
+// 256-token chunk after 3840 cached tokens runs in 149 us against 171 on the
+// single kernel, while 1024-token prompts without prefix ran 237 -> 298 us
+// on the paired kernel's first version.
 template <bool BF16>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   CUtensorMap km, vm, qm;
@@ -1173,8 +1202,8 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
       (long long)a.num_seqs * a.num_kv_heads * (pair ? (a.num_partitions + 1) / 2 : a.num_partitions);
   const int grid = (int)(units < sms ? units : sms);
   return launch_pdl(pair ? prefill_pair_kernel<BF16> : prefill_single_kernel<BF16>, dim3(grid),
-                    dim3(kThreads), pair ? smem_bytes<true>() : smem_bytes<false>(), st, km, vm,
-                    qm, a);
+                    dim3(pair ? kThreadsPair : kThreads), pair ? smem_bytes<true>() : smem_bytes<false>(),
+                    st, km, vm, qm, a);
 }
 
 }  // namespace
