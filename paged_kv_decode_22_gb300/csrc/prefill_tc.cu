@@ -8,7 +8,7 @@
 // Query tile = QT = 128 / g chunk queries of one (sequence, KV head): its 128
 // rows are the (query, head) pairs r = query * g + head, so all g heads of a
 // query share every K/V tile.  Two kernels, both persistent (one CTA per
-// SM, units dealt round-robin, heaviest first), 8 warps:
+// SM, units dealt round-robin, heaviest first):
 //   warps 0, 3 K producers (half 0 and the unit's Q tiles; half 1): TMA boxes
 //              of one block x 64 columns into a ring of 32 KB stages, block
 //              ids one tile ahead, out-of-range blocks from an
@@ -19,26 +19,30 @@
 //                            A = Q (shared memory), B = K tile, into TMEM;
 //                O += P V    M = 128 rows, N = head_size, K = 128 tokens,
 //                            A = P (TMEM, written by the softmax), B = V tile.
-//   warps 4-7  softmax: thread = TMEM lane = one row.  The row's 128 logits
-//              of a tile are in registers, so its maximum and sum need no
-//              other thread.  p = 2^(x - m_ref) with a reference maximum
-//              m_ref that moves only when a logit passes it by more than 8
-//              (log2 units); then l and the row of O (in TMEM) are rescaled.
-//              P goes back into TMEM as 16-bit pairs over the first 64
+//   softmax    thread = TMEM lane = one row.  The row's 128 logits of a
+//              tile are in registers, so its maximum and sum need no other
+//              thread.  p = 2^(x - m_ref) with a reference maximum m_ref
+//              that moves only when a logit passes it by more than 8 (log2
+//              units); then l and the row of O (in TMEM) are rescaled.  P
+//              goes back into TMEM as 16-bit pairs over the first 64
 //              columns of the tile's S.
-// Single kernel: a unit is one query tile; S double-buffered by tile parity
-// and O by unit parity (512 TMEM columns), so a unit's output is written
-// after the next unit's first P.
-// Paired kernel: a unit is TWO consecutive query tiles (slots A and B) of
-// one (sequence, KV head) and every K/V tile serves both, so a tile carries
-// twice the MMA work it costs in TMA boxes and a CTA switches units half as
-// often.  TMEM holds S_A, S_B, O_A, O_B; the MMA order per K/V tile is S_A
-// S_B | P_A V, next S_A | P_B V, next S_B, so that each slot's next S runs
-// while the softmax works on the other slot.  Its softmax is two
-// warpgroups (12 warps in all): the two threads of a row each take 64 of its
-// 128 columns and agree on the row maximum through shared memory.  A unit
-// whose second tile does not exist (the last of an odd count) runs slot A
-// only.
+// Single kernel (8 warps, softmax warps 4-7): a unit is one query tile; S
+// double-buffered by tile parity and O by unit parity (512 TMEM columns),
+// so a unit's output is written after the next unit's first P.
+// Paired kernel (12 warps): a unit is TWO consecutive query tiles (slots A
+// and B) of one (sequence, KV head) and every K/V tile serves both, so a
+// tile carries twice the MMA work it costs in TMA boxes and a CTA switches
+// units half as often.  TMEM holds S_A, S_B, O_A, O_B; the MMA order per
+// K/V tile is S_A S_B | P_A V, next S_A | P_B V, next S_B, so that each
+// slot's next S runs while the softmax works on the other slot.  Warps 4-7
+// run slot A's softmax and warps 8-11 slot B's, each at its own pace (the
+// pattern of FlashAttention-4's two softmax warpgroups).  Per tile a thread
+// loads its 128 logits with one TMEM load, takes the maximum with
+// three-input max instructions, and scales and sums on packed f32 pairs;
+// it settles the K stage's bookkeeping after handing over P.  The
+// producers' path from a stage's release to its TMA issue holds no warp
+// exchange.  A unit whose second tile does not exist (the last of an odd
+// count) runs slot A only.
 #include <cuda.h>
 
 #include <atomic>
@@ -63,6 +67,7 @@ constexpr int kPfTable = 128;            // sequences whose lengths and chunk bo
 constexpr int kThreads = 256;            // single kernel: 8 warps
 constexpr int kThreadsPair = 384;        // paired kernel: 12 warps (two softmax warpgroups)
 constexpr int kSoftmaxThreads = 128;
+constexpr int kMaxBox = TT / 8;          // boxes per tile and half at the smallest block size (8)
 constexpr int kNoBlock = -2147483647 - 1;
 constexpr float kHeadroom = 8.f;         // log2 units: p < 2^8 between rescales
 constexpr int kPairMinTokens = 1024;     // paired kernel from this many visible tokens per query
@@ -74,7 +79,7 @@ __host__ __device__ constexpr uint32_t col_o(int x) { return x ? 384u : 256u; }
 // paired kernel's slots A and B), the K ring, the V ring, then the barriers.
 template <bool PAIR>
 struct Layout {
-  static constexpr int NK = 2;
+  static constexpr int NK = PAIR ? 3 : 2;   // K ring stages
   static constexpr int off_q = 0;
   static constexpr int off_k = off_q + 2 * Q_BYTES;
   static constexpr int off_v = off_k + NK * TILE_BYTES;
@@ -89,11 +94,9 @@ struct PfTab {
 };
 
 constexpr int kMiscBytes = 1280;          // single kernel
-constexpr int kMiscBytesPair = 5376;      // paired kernel (+ the halves' maxima and sums)
+constexpr int kMiscBytesPair = 1280;      // paired kernel
 struct MiscPair {
   uint64_t k_full[Layout<true>::NK], k_empty[Layout<true>::NK], v_full[NV], v_empty[NV];
-  float xm[2][2][128];   // row maxima of the two column halves, [buffer][half][row]
-  float xl[2][2][128];   // row sums of the two column halves, [slot][half][row]
   // per slot (A, B)
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2], o_full[2];
   uint64_t drain;
@@ -705,7 +708,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       mbar_init(&ms.q_full[x], 1);
       mbar_init(&ms.q_empty[x], 1);
       mbar_init(&ms.s_full[x], 1);
-      mbar_init(&ms.p_full[x], 2 * kSoftmaxThreads);
+      mbar_init(&ms.p_full[x], kSoftmaxThreads);
       mbar_init(&ms.pv_done[x], 1);
       mbar_init(&ms.o_full[x], 1);
     }
@@ -749,9 +752,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const int my_box = lane % nbox, my_half = lane / nbox;
     auto load_raw = [&](const PairUnit& t, int tj) {
       int raw = kNoBlock;
-      if (lane < nbox) {
+      if (lane < 2 * nbox) {
         const int ts = tj * TT;
-        const int tok0 = B <= TT ? ts + lane * B : ts;
+        const int tok0 = B <= TT ? ts + my_box * B : ts;
         if (tok0 < t.t1) raw = __ldg(a.block_tables + (size_t)t.s * a.max_blocks_per_seq + tok0 / B);
       }
       return raw;
@@ -796,24 +799,27 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       const int ts = jl * TT;
       const bool bad = raw != kNoBlock && (raw < 0 || raw >= a.num_blocks);
       const int row = (raw != kNoBlock && !bad) ? raw * B + (B <= TT ? 0 : ts % B) : oob_row;
-      const uint32_t bad_lanes = __ballot_sync(0xffffffffu, bad);   // lanes < nbox: boxes in token order
+      // lanes < nbox: boxes in token order
+      const uint32_t bad_lanes = __ballot_sync(0xffffffffu, bad && lane < nbox);
       const int st = jk % nst;
-      if (lane == 0) {
-        ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
-        if (ok && primary) {
-          if (!is_v) {
-            ms.k_bad[st] = bad_lanes ? (__ffs(bad_lanes) - 1) * R : -1;
-            if (bad_lanes) flag(a.status, PKD_DEV_BAD_BLOCK);
-          }
-          mbar_arrive_expect_tx(&full[st], TILE_BYTES);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // Every lane polls the stage barrier, and each issuer lane holds its
+      // own box's row: nothing on the way from the stage's release to the
+      // TMA issue is a warp exchange.  The stage's transaction count may
+      // go below zero until lane 0's expect-tx arrives; its one pending
+      // arrival keeps the phase open until then.
+      ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      const int r = __shfl_sync(0xffffffffu, row, my_box);
       if (issuer) {
         uint8_t* dst = ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128;
-        tma_load_3d(dst, map, &full[st], my_half * 64, pu.hk, r);
+        tma_load_3d(dst, map, &full[st], my_half * 64, pu.hk, row);
+      }
+      if (lane == 0 && primary) {
+        if (!is_v) {
+          ms.k_bad[st] = bad_lanes ? (__ffs(bad_lanes) - 1) * R : -1;
+          if (bad_lanes) flag(a.status, PKD_DEV_BAD_BLOCK);
+        }
+        mbar_arrive_expect_tx(&full[st], TILE_BYTES);
       }
       ++jk;
       if (njl == 0) {
@@ -929,37 +935,172 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ============================================================ softmax / epilogue
-    // Two warpgroups: warp 4 + q and warp 8 + q share TMEM lanes 32q..32q+31
-    // (rows); warpgroup h takes columns [64h, 64h + 64) of S (tokens) and of
-    // O (head dims).  The two threads of a row agree on its maximum through
-    // shared memory and one 64-thread named barrier per tile; every barrier
-    // also ANDs their `ok`, so the two stop together.
+    // Warpgroup x (warps 4-7: slot A, warps 8-11: slot B) works on its own
+    // slot's tiles: thread = TMEM lane = one row, the row's 128 logits of a
+    // tile in its registers.  The two warpgroups are coupled only through
+    // the MMA order, so on every SM sub-partition one warp's exponentials
+    // overlap the other's TMEM loads and reductions.
     const int wq = warp & 3;                   // TMEM lane quadrant
-    const int hh = (warp - 4) >> 2;            // column half
-    const int row = wq * 32 + lane;            // this thread's row of S, P and O (both slots)
-    const uint32_t bar = 1 + wq;               // named barrier of this row quadrant's two warps
+    const int x = (warp - 4) >> 2;             // slot of this warpgroup
+    const int row = wq * 32 + lane;            // this thread's row of S, P and O
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t s_addr = lane_addr + col_s(x), o_addr = lane_addr + col_o(x);
     const float qscale = a.scale * kLog2e;
     const int H = a.num_heads;
     const int qi = row / g, hj = row - qi * g; // row = (tile query qi, head hj of the group)
     const bool alibi = a.alibi != nullptr;
-    uint32_t j = 0, jb = 0, un = 0, unb = 0;
+    const bool fold = !alibi && qscale > 0.f;
+    const float sc = fold ? qscale : 1.f;
+    uint32_t j = 0, jx = 0, ux = 0;            // tiles of all units, tiles and units of this slot
     bool ok = true;
-    // Write this thread's half of slot x's row of a finished unit (output
-    // row `orow`, -1 for an invalid row): wait for the slot's last P V, read
-    // O_x from TMEM, scale by `inv`, store 16-bit.
-    auto finalize = [&](int x, uint32_t phase, long long orow, float inv) {
-      ok = ok && mbar_wait(&ms.o_full[x], phase & 1);
-      if (!ok) return;
-      tc_fence_after();
-      const bool wr = orow >= 0;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + (size_t)(wr ? orow : 0) * HD +
-                                            hh * 64);
+    PairCursor cur;
+    cur.begin(a);
+    PairUnit pu;
+    while (ok && cur.step(ms.tab, a, pu)) {
+      // Slot B of a unit without a second query tile has no work, but its
+      // warpgroup still releases every K stage the unit uses.
+      const bool mine = x == 0 || pu.hasB;
+      const bool valid = mine && qi < pu.nq[x];
+      const int pos = valid ? pu.pos0[x] + qi : -1;         // last visible token
+      const float slope = alibi && valid ? a.alibi[pu.hk * g + hj] * kLog2e : 0.f;
+      float m_ref = valid ? -INFINITY : INFINITY;           // +inf: p = 0, never rescales
+      float l = 0.f;
+      int bad_from = 0x7fffffff;
+      for (int jl = 0; jl < pu.ntiles; ++jl, ++j) {
+        const int ks = j % Layout<true>::NK;
+        const int ts = jl * TT;
+        // The K stage's bad-block entry, then the stage's release (the
+        // MMA's commit is its other arrival).  A slot with work does this
+        // after handing over the tile's P, off the path from S to P.
+        auto release_k = [&]() {
+          ok = ok && mbar_wait(&ms.k_full[ks], (j / Layout<true>::NK) & 1);
+          if (ok) {
+            const int kb = ms.k_bad[ks];
+            if (kb >= 0) bad_from = min(bad_from, ts + kb);
+          }
+          mbar_arrive(&ms.k_empty[ks]);
+        };
+        if (!mine) {
+          release_k();
+          if (!ok) break;
+          continue;
+        }
+        ok = ok && mbar_wait(&ms.s_full[x], jx & 1);
+        if (!ok) break;
+        tc_fence_after();
+        // This row's logits for the tile, log2 units, masked past the query,
+        // one 64-column half at a time: the second half for its maximum, the
+        // first (kept) for its maximum and exponentials, then the second
+        // again.  Without ALiBi the scale folds into the exponent's FMA (sc =
+        // scale * log2 e > 0: the maximum of xv is the maximum of the
+        // logits); with ALiBi xv carries the scale and the bias.
+        float xv[TT];
+        tmem_ld128(s_addr, xv);
+        if (!fold) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+          for (int i = 0; i < TT; ++i) {
+            const int t = ts + i;
+            xv[i] = t <= pos ? fmaf(xv[i], qscale, slope * (float)(t - pos)) : -INFINITY;
+          }
+        } else if (ts + TT - 1 > pos) {         // the tile passes this row's query
+#pragma unroll
+          for (int i = 0; i < TT; ++i) xv[i] = ts + i <= pos ? xv[i] : -INFINITY;
+        }
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(xv[k], xv[8 + k]);
+#pragma unroll
+        for (int i = 16; i < TT; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], xv[i + k], xv[i + 8 + k]);
+        const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7]))) * sc;
+        float alpha = 1.f;
+        if (mx > m_ref + kHeadroom) {
+          const float m_new = fmaxf(m_ref, mx);
+          alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m_new);
+          l *= alpha;
+          m_ref = m_new;
+        }
+        // Rows whose reference moved rescale their O (accumulated in TMEM by
+        // the slot's previous P V) once that P V has completed.
+        if (__any_sync(0xffffffffu, alpha != 1.f && jl > 0)) {
+          ok = ok && mbar_wait(&ms.pv_done[x], (jx - 1) & 1);
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 16; ++c) {
+            float v[16];
+            uint32_t w[16];
+            tmem_ld16(o_addr + c * 16, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * alpha);
+            tmem_st16(o_addr + c * 16, w);
+          }
+          tmem_wait_st();
+        }
+        // P = 2^(xv * sc - m_ref), 16-bit pairs over the S buffer's first 64
+        // columns (half h's into columns [32h, 32h + 32), which held only
+        // first-half logits).  The scaling and the row sum run on packed
+        // pairs (one instruction for two values), the sum in 4 independent
+        // pair chains.
+        const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t l2[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 es = f2_unpack(f2_fma(f2_pack(xv[32 * c + 2 * i], xv[32 * c + 2 * i + 1]), sc2, nm2));
+            const uint64_t p2 = f2_pack(fast_exp2(es.x), fast_exp2(es.y));
+            l2[i & 3] = f2_add(l2[i & 3], p2);
+            const float2 ps = f2_unpack(p2);
+            w[i] = pack2<BF16>(ps.x, ps.y);
+          }
+          tmem_st16(s_addr + c * 16, w);
+        }
+        {
+          const float2 lt = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));
+          l += lt.x + lt.y;
+        }
+        // Cache slots past the sequence end inside a loaded block may hold
+        // anything (NaN included): slot A's warpgroup zeroes those V rows
+        // before its P V, the first to read the tile (thread `row` clears
+        // token row `row`).
+        if (x == 0 && ts + TT > pu.L) {
+          const int vs = j % NV;
+          ok = ok && mbar_wait(&ms.v_full[vs], (j / NV) & 1);
+          if (ok && ts + row >= pu.L) {
+            uint4* v0 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + row * 128);
+            uint4* v1 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + TT * 128 + row * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v0[i] = v1[i] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&ms.p_full[x]);
+        release_k();
+        if (!ok) break;
+        ++jx;
+      }
+      if (!ok) break;
+      if (!mine) continue;
+      // ---------------------------------------------------------- finish the unit
+      // Wait for the slot's last P V, then write this row of O / l.  The
+      // next unit's first P V (which overwrites O) waits for this
+      // warpgroup's next P, so O is read before it is reused.
+      ok = mbar_wait(&ms.o_full[x], ux & 1);
+      if (!ok) break;
+      tc_fence_after();
+      const float inv = !valid || pos >= bad_from || l == 0.f ? 0.f : 1.f / l;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                            ((size_t)(valid ? pu.qrow0[x] + qi : 0) * H +
+                                             pu.hk * g + hj) * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
         float v[32];
-        tmem_ld32(lane_addr + col_o(x) + hh * 64 + c * 32, v);
-        if (wr) {
+        tmem_ld32(o_addr + c * 32, v);
+        if (valid) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[c * 4 + i] = make_uint4(pack2<BF16>(v[8 * i] * inv, v[8 * i + 1] * inv),
@@ -969,184 +1110,9 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         }
       }
       tc_fence_before();
-    };
-    // Slot B of a finished unit is written after the next unit's first P_A
-    // (its last P V, issued after the unit's last P_B, completes meanwhile).
-    bool pend = false;
-    uint32_t pend_phase = 0;
-    long long pend_row = -1;
-    float pend_inv = 0.f;
-    auto out_row = [&](bool valid, int qrow0, int hk) {
-      return valid ? (long long)(qrow0 + qi) * H + hk * g + hj : -1ll;
-    };
-    auto inv_of = [&](bool valid, int pos, float lx, int bad_from) {
-      return !valid || pos >= bad_from || lx == 0.f ? 0.f : 1.f / lx;
-    };
-    PairCursor cur;
-    cur.begin(a);
-    PairUnit pu;
-    while (ok && cur.step(ms.tab, a, pu)) {
-      const bool hb = pu.hasB;
-      // Per slot (A, B): row validity, position (last visible token),
-      // reference maximum (+inf: p = 0, never rescales) and this half's sum;
-      // the slope is the row's head's, the first bad token the unit's.
-      const bool valid_a = qi < pu.nq[0], valid_b = hb && qi < pu.nq[1];
-      const int pos_a = valid_a ? pu.pos0[0] + qi : -1, pos_b = valid_b ? pu.pos0[1] + qi : -1;
-      const float slope = alibi ? a.alibi[pu.hk * g + hj] * kLog2e : 0.f;
-      float m_a = valid_a ? -INFINITY : INFINITY, m_b = valid_b ? -INFINITY : INFINITY;
-      float l_a = 0.f, l_b = 0.f;
-      int bad_from = 0x7fffffff;
-      for (int jl = 0; jl < pu.ntiles; ++jl, ++j) {
-        const int ks = j % Layout<true>::NK;
-        const int ts = jl * TT;
-        const int tc0 = ts + hh * 64;          // first token of this thread's columns
-#pragma unroll 1
-        for (int x = 0; x < 2; ++x) {
-          if (x == 1 && !hb) break;
-          const uint32_t jx = x == 0 ? j : jb + jl;   // this slot's tile count (barrier phase)
-          const int p_x = x ? pos_b : pos_a;
-          float m_ref = x ? m_b : m_a, l_x = x ? l_b : l_a;
-          ok = ok && mbar_wait(&ms.s_full[x], jx & 1);
-          if (x == 0) {
-            ok = ok && mbar_wait(&ms.k_full[ks], (j / Layout<true>::NK) & 1);
-            if (ok) {
-              tc_fence_after();
-              const int kb = ms.k_bad[ks];
-              if (kb >= 0) bad_from = min(bad_from, ts + kb);
-            }
-            mbar_arrive(&ms.k_empty[ks]);
-          }
-          tc_fence_after();
-          // This half row's logits for the tile, log2 units, masked past the query.
-          float xv[64];
-          const bool fold = !alibi && qscale > 0.f;
-          const float sc = fold ? qscale : 1.f;
-          float mpart = -INFINITY;
-          if (ok) {
-            tmem_ld64(lane_addr + col_s(x) + hh * 64, xv);
-            // Without ALiBi the scale folds into the exponent's FMA (sc =
-            // scale * log2 e > 0: the maximum of x is the maximum of the
-            // logits); with ALiBi x carries the scale and the bias.
-            if (!fold) {
-#pragma unroll
-              for (int i = 0; i < 64; ++i) {
-                const int t = tc0 + i;
-                xv[i] = t <= p_x ? fmaf(xv[i], qscale, slope * (float)(t - p_x)) : -INFINITY;
-              }
-            } else if (tc0 + 63 > p_x) {         // the half passes this row's query
-#pragma unroll
-              for (int i = 0; i < 64; ++i) xv[i] = tc0 + i <= p_x ? xv[i] : -INFINITY;
-            }
-            float m4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) m4[k] = xv[k];
-#pragma unroll
-            for (int i = 4; i < 64; i += 4)
-#pragma unroll
-              for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], xv[i + k]);
-            mpart = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          }
-          // The row maximum: this half's and the other's.
-          const int xb = hb ? x : (jl & 1);
-          ms.xm[xb][hh][row] = mpart;
-          ok = named_barrier_and(bar, 64, ok);
-          if (!ok) break;
-          const float mx = fmaxf(mpart, ms.xm[xb][hh ^ 1][row]) * sc;
-          float alpha = 1.f;
-          if (mx > m_ref + kHeadroom) {
-            const float m_new = fmaxf(m_ref, mx);
-            alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m_new);
-            l_x *= alpha;
-            m_ref = m_new;
-          }
-          // Rows whose reference moved rescale their O (accumulated in TMEM
-          // by the slot's previous P V) once that P V has completed; each
-          // thread its half of the row.
-          if (__any_sync(0xffffffffu, alpha != 1.f && jl > 0)) {
-            ok = ok && mbar_wait(&ms.pv_done[x], (jx - 1) & 1);
-            tc_fence_after();
-            const uint32_t o_addr = lane_addr + col_o(x) + hh * 64;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float v[16];
-              uint32_t w[16];
-              tmem_ld16(o_addr + c * 16, v);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * alpha);
-              tmem_st16(o_addr + c * 16, w);
-            }
-            tmem_wait_st();
-          }
-          // P = 2^(x * sc - m_ref) for this half's 64 tokens: 16-bit pairs in
-          // S columns [32h, 32h + 32); the half's sum in 4 chains.
-          {
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float p0 = fast_exp2(fmaf(xv[2 * i], sc, -m_ref));
-              const float p1 = fast_exp2(fmaf(xv[2 * i + 1], sc, -m_ref));
-              l4[(2 * i) & 3] += p0;
-              l4[(2 * i + 1) & 3] += p1;
-              w[i] = pack2<BF16>(p0, p1);
-            }
-            tmem_st32(lane_addr + col_s(x) + hh * 32, w);
-            l_x += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-          }
-          if (x) {
-            m_b = m_ref;
-            l_b = l_x;
-          } else {
-            m_a = m_ref;
-            l_a = l_x;
-          }
-          // Cache slots past the sequence end inside a loaded block may hold
-          // anything (NaN included): zero those V rows before either P V
-          // reads them (this thread clears its half of token row `row`).
-          if (x == 0 && ts + TT > pu.L) {
-            const int vs = j % NV;
-            ok = ok && mbar_wait(&ms.v_full[vs], (j / NV) & 1);
-            if (ok && ts + row >= pu.L) {
-              uint4* v0 = reinterpret_cast<uint4*>(vbuf + vs * TILE_BYTES + hh * TT * 128 + row * 128);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v0[i] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&ms.p_full[x]);
-          if (x == 0 && pend) {
-            // The previous unit's slot B: its sums were exchanged at that
-            // unit's end.
-            pend = false;
-            finalize(1, pend_phase, pend_row, pend_inv);
-          }
-        }
-        if (!ok) break;
-      }
-      // ---------------------------------------------------------- finish the unit
-      // Exchange the halves' sums; slot A now (its last P V ran during slot
-      // B's softmax), slot B after the next unit's first P_A.
-      ms.xl[0][hh][row] = l_a;
-      if (hb) ms.xl[1][hh][row] = l_b;
-      ok = named_barrier_and(bar, 64, ok);
-      if (!ok) break;
-      finalize(0, un, out_row(valid_a, pu.qrow0[0], pu.hk),
-               inv_of(valid_a, pos_a, l_a + ms.xl[0][hh ^ 1][row], bad_from));
-      if (hb) {
-        pend = true;
-        pend_phase = unb;
-        pend_row = out_row(valid_b, pu.qrow0[1], pu.hk);
-        pend_inv = inv_of(valid_b, pos_b, l_b + ms.xl[1][hh ^ 1][row], bad_from);
-        jb += pu.ntiles;
-        ++unb;
-      }
-      ++un;
-      ok = named_barrier_and(bar, 64, ok);   // both threads go on together
+      ++ux;
     }
-    if (ok && pend) finalize(1, pend_phase, pend_row, pend_inv);
-    if (!ok && threadIdx.x == 128) set_abort(ms, a.status);
+    if (!ok) set_abort(ms, a.status);
   }
 
   // ---------------------------------------------------------------- teardown
