@@ -307,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_box = lane % nbox, my_half = lane / nbox;
     auto load_raw = [&](const UnitInfo& t, int tj) {
       int raw = kNoBlock;
-      if (lane < nbox) {
+      if (lane < 2 * nbox) {
         const int ts = tj * TT;
-        const int tok0 = B <= TT ? ts + lane * B : ts;
+        const int tok0 = B <= TT ? ts + my_box * B : ts;
         if (tok0 < t.t1) raw = __ldg(a.block_tables + (size_t)t.s * a.max_blocks_per_seq + tok0 / B);
       }
       return raw;
@@ -345,24 +345,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ts = jl * TT;
       const bool bad = raw != kNoBlock && (raw < 0 || raw >= a.num_blocks);
       const int row = (raw != kNoBlock && !bad) ? raw * B + (B <= TT ? 0 : ts % B) : oob_row;
-      const uint32_t bad_lanes = __ballot_sync(0xffffffffu, bad);   // lanes < nbox: boxes in token order
+      // lanes < nbox: boxes in token order
+      const uint32_t bad_lanes = __ballot_sync(0xffffffffu, bad && lane < nbox);
       const int st = jk % nst;
-      if (lane == 0) {
-        ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
-        if (ok && primary) {
-          if (!is_v) {
-            ms.k_bad[st] = bad_lanes ? (__ffs(bad_lanes) - 1) * R : -1;
-            if (bad_lanes) flag(a.status, PKD_DEV_BAD_BLOCK);
-          }
-          mbar_arrive_expect_tx(&full[st], TILE_BYTES);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // Every lane polls the stage barrier, and each issuer lane holds its
+      // own box's row: nothing on the way from the stage's release to the
+      // TMA issue is a warp exchange.  The stage's transaction count may
+      // go below zero until lane 0's expect-tx arrives; its one pending
+      // arrival keeps the phase open until then.
+      ok = ok && mbar_wait(&empty[st], ((jk / nst) & 1) ^ 1);
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      const int r = __shfl_sync(0xffffffffu, row, my_box);
       if (issuer) {
         uint8_t* dst = ring + st * TILE_BYTES + my_half * TT * 128 + my_box * R * 128;
-        tma_load_3d(dst, map, &full[st], my_half * 64, ui.hk, r);
+        tma_load_3d(dst, map, &full[st], my_half * 64, ui.hk, row);
+      }
+      if (lane == 0 && primary) {
+        if (!is_v) {
+          ms.k_bad[st] = bad_lanes ? (__ffs(bad_lanes) - 1) * R : -1;
+          if (bad_lanes) flag(a.status, PKD_DEV_BAD_BLOCK);
+        }
+        mbar_arrive_expect_tx(&full[st], TILE_BYTES);
       }
       ++jk;
       if (njl == 0) ++un;
@@ -499,23 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1, ks = j % Layout<false>::NK;
         const int ts = jl * TT;
         ok = ok && mbar_wait(&ms.s_full[b], (j >> 1) & 1);
-        ok = ok && mbar_wait(&ms.k_full[ks], (j / Layout<false>::NK) & 1);
         if (!ok) break;
         tc_fence_after();
-        {
-          const int kb = ms.k_bad[ks];
-          if (kb >= 0) bad_from = min(bad_from, ts + kb);
-        }
-        mbar_arrive(&ms.k_empty[ks]);
         // This row's logits for the tile, log2 units, masked past the query.
         float x[TT];
-#pragma unroll
-        for (int c = 0; c < TT / 32; ++c) {
-          float v[32];
-          tmem_ld32(lane_addr + b * 128 + c * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = v[i];
-        }
+        tmem_ld128(lane_addr + b * 128, x);
         // Logits in log2 units are x * sc: without ALiBi the scale folds into
         // the exponent's FMA (sc = scale * log2 e > 0: the maximum of x is the
         // maximum of the logits); with ALiBi x carries the scale and the bias.
@@ -531,16 +522,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < TT; ++i) x[i] = ts + i <= pos ? x[i] : -INFINITY;
         }
-        // Row maximum: 8 independent chains, then a 3-level tree.
+        // Row maximum: 8 independent chains of three-input maxima, then a
+        // tree.
         float m8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = x[k];
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(x[k], x[8 + k]);
 #pragma unroll
-        for (int i = 8; i < TT; i += 8)
+        for (int i = 16; i < TT; i += 16)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], x[i + k]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sc;
+          for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], x[i + k], x[i + 8 + k]);
+        const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7]))) * sc;
         float alpha = 1.f;
         if (mx > m_ref + kHeadroom) {
           const float m_new = fmaxf(m_ref, mx);
@@ -567,22 +558,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         // P = 2^(x * sc - m_ref), 16-bit pairs over the S buffer's first 64
-        // columns; the row sum in 8 independent chains.
-        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // columns.  The scaling and the row sum run on packed pairs (one
+        // instruction for two values), the sum in 4 independent pair chains.
+        const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t l2[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t w[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sc, -m_ref));
-            const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sc, -m_ref));
-            l8[(2 * i) & 7] += p0;
-            l8[(2 * i + 1) & 7] += p1;
-            w[i] = pack2<BF16>(p0, p1);
+            const float2 es = f2_unpack(f2_fma(f2_pack(x[c * 64 + 2 * i], x[c * 64 + 2 * i + 1]), sc2, nm2));
+            const uint64_t p2 = f2_pack(fast_exp2(es.x), fast_exp2(es.y));
+            l2[i & 3] = f2_add(l2[i & 3], p2);
+            const float2 ps = f2_unpack(p2);
+            w[i] = pack2<BF16>(ps.x, ps.y);
           }
           tmem_st32(lane_addr + b * 128 + c * 32, w);
         }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        {
+          const float2 lt = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));
+          l += lt.x + lt.y;
+        }
         // Cache slots past the sequence end inside a loaded block may hold
         // anything (NaN included): zero those V rows before P V reads them
         // (thread `row` clears token row `row` of the tile).
@@ -600,6 +596,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ms.p_full[b]);
+        // The K stage's bad-block entry, then the stage's release (the
+        // MMA's commit is its other arrival), off the path from S to P.
+        ok = ok && mbar_wait(&ms.k_full[ks], (j / Layout<false>::NK) & 1);
+        if (ok) {
+          const int kb = ms.k_bad[ks];
+          if (kb >= 0) bad_from = min(bad_from, ts + kb);
+        }
+        mbar_arrive(&ms.k_empty[ks]);
+        if (!ok) break;
         if (pend) finalize();   // the previous unit's output, its last P V now done
       }
       if (!ok) break;
