@@ -1026,22 +1026,6 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
           l *= alpha;
           m_ref = m_new;
         }
-        // Rows whose reference moved rescale their O (accumulated in TMEM by
-        // the slot's previous P V) once that P V has completed.
-        if (__any_sync(0xffffffffu, alpha != 1.f && jl > 0)) {
-          ok = ok && mbar_wait(&ms.pv_done[x], (jx - 1) & 1);
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < HD / 16; ++c) {
-            float v[16];
-            uint32_t w[16];
-            tmem_ld16(o_addr + c * 16, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * alpha);
-            tmem_st16(o_addr + c * 16, w);
-          }
-          tmem_wait_st();
-        }
         // P = 2^(xv * sc - m_ref), 16-bit pairs over the S buffer's first 64
         // columns (half h's into columns [32h, 32h + 32), which held only
         // first-half logits).  The scaling and the row sum run on packed
@@ -1065,6 +1049,24 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         {
           const float2 lt = f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])));
           l += lt.x + lt.y;
+        }
+        // Rows whose reference moved rescale their O (accumulated in TMEM by
+        // the slot's previous P V) once that P V has completed, before this
+        // tile's P V: after the exponentials, when the logits no longer
+        // hold registers.
+        if (__any_sync(0xffffffffu, alpha != 1.f && jl > 0)) {
+          ok = ok && mbar_wait(&ms.pv_done[x], (jx - 1) & 1);
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 16; ++c) {
+            float v[16];
+            uint32_t w[16];
+            tmem_ld16(o_addr + c * 16, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(v[i] * alpha);
+            tmem_st16(o_addr + c * 16, w);
+          }
+          tmem_wait_st();
         }
         // Cache slots past the sequence end inside a loaded block may hold
         // anything (NaN included): slot A's warpgroup zeroes those V rows
