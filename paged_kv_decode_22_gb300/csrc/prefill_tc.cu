@@ -67,7 +67,6 @@ constexpr int kPfTable = 128;            // sequences whose lengths and chunk bo
 constexpr int kThreads = 256;            // single kernel: 8 warps
 constexpr int kThreadsPair = 384;        // paired kernel: 12 warps (two softmax warpgroups)
 constexpr int kSoftmaxThreads = 128;
-constexpr int kMaxBox = TT / 8;          // boxes per tile and half at the smallest block size (8)
 constexpr int kNoBlock = -2147483647 - 1;
 constexpr float kHeadroom = 8.f;         // log2 units: p < 2^8 between rescales
 constexpr int kPairMinTokens = 1024;     // paired kernel from this many visible tokens per query
