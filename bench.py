@@ -17,7 +17,9 @@ Prints ONE JSON line (rank 0).  `value` is algorithmic HBM bytes per step
 lengths) divided by device time per step, GB/s (1e9).  The KV pool is 33x
 the L2, so every step streams its inputs from HBM.  Beside it: `e2e` (the
 same call with q, tables and lengths copied in from pinned host memory and
-out copied back, every step), `roofline` against the measured copy
+out copied back, every step, the steps pipelined as a serving loop runs
+them: one step's copies overlap the neighbouring steps' calls), `roofline`
+against the measured copy
 bandwidth, `cpu_baseline` (the float64 oracle on a sample of the same
 workload, one core and all cores), and side lines for the other decode
 workloads, gather_cached_kv and prefill.
@@ -731,30 +733,57 @@ def main():
     # End to end through the public API with host buffers: every step copies
     # q, the block tables and the lengths in from pinned host memory, runs the
     # call and copies out back to pinned host memory.  The KV pool is resident
-    # state, as in serving.
+    # state, as in serving.  Steps are pipelined as a serving loop runs them:
+    # two sets of device inputs and outputs, step i + 1's inputs come in on
+    # one copy stream and step i's output goes out on another while a call
+    # runs; each call waits for its own inputs, and each buffer set is reused
+    # only after its call and its output copy are done.  The timed region
+    # ends when the last output has reached the host.
     hq = d["q"].cpu().pin_memory()
     hbt = d["bt"].cpu().pin_memory()
     hcl = d["cl"].cpu().pin_memory()
-    hout = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
+    hout = [torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hcl))
-    d2h = hout.numel() * hout.element_size()
+    d2h = hout[0].numel() * hout[0].element_size()
+    bufs = [{k: d[k] for k in ("q", "bt", "cl", "out")},
+            {k: torch.empty_like(d[k]) for k in ("q", "bt", "cl", "out")}]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer set b landed
+    ev_call = [torch.cuda.Event() for _ in range(2)]   # call on buffer set b done
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # output of buffer set b on the host
+    nstep = [0]
 
     def e2e_step():
-        d["q"].copy_(hq, non_blocking=True)
-        d["bt"].copy_(hbt, non_blocking=True)
-        d["cl"].copy_(hcl, non_blocking=True)
-        call()
-        hout.copy_(d["out"], non_blocking=True)
-        stream.synchronize()
+        b = nstep[0] & 1
+        nstep[0] += 1
+        x = bufs[b]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_call[b])          # the previous call on this set has read its inputs
+            x["q"].copy_(hq, non_blocking=True)
+            x["bt"].copy_(hbt, non_blocking=True)
+            x["cl"].copy_(hcl, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])             # this set's previous output has left
+        ops.paged_decode_attention(x["out"], x["q"], d["kc"], d["vc"], x["bt"], x["cl"],
+                                   d["max_ctx"], d["scale"], workspace=work, stream=stream)
+        ev_call[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_call[b])
+            hout[b].copy_(x["out"], non_blocking=True)
+            ev_out[b].record(s_out)
 
-    for _ in range(3):
+    for _ in range(4):
         e2e_step()
     barrier()
     t0 = time.perf_counter()
     timed_loop(e2e_step, args.steps, lambda i: None)
-    barrier()
+    barrier()                                    # every stream, the last output copy included
     e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dist, dev)
-    del d, work
+    # The pipelined outputs are the same call's: check the last one.
+    if not torch.equal(hout[(nstep[0] - 1) & 1], d["out"].cpu()):
+        raise RuntimeError("pipelined end-to-end output differs from the device-timed call's")
+    del d, work, bufs
     torch.cuda.empty_cache()
 
     sides = None
@@ -790,7 +819,9 @@ def main():
                      "traffic": traffic, "algorithmic_bytes": step_bytes},
         "e2e": {"value": round(whole_job_gbps(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "pipelining": "two device buffer sets; each step's host copies run on two copy "
+                              "streams beside the neighbouring steps' calls"},
         "clocks": clocks.summary(),
     }
     if sides is not None:
