@@ -75,6 +75,10 @@ struct DecodeArgs {
                         // s * Hk + hk, total positions T}; n = 0 when no pair is cut there
   const int32_t* query_start;   // prefill: [S + 1] cumulative chunk lengths (nullptr: decode)
   int q_per_unit;       // prefill: query tokens per work unit
+  // prefill: the grid stride gridDim.x written as (ds * Hk + dhk) * per + dr,
+  // per the units per (sequence, KV head) of the launched kernel (set by the
+  // launch, so that a CTA's walk over its units needs no division)
+  int walk_dr, walk_dhk, walk_ds;
   int max_query_len;    // prefill: longer chunks are invalid (zero rows)
   int num_q_tokens;     // prefill: rows of q and out (query_start[S])
   float* ws_o;          // [S][Hk][P][H/Hk][D] unnormalised partial outputs

@@ -90,10 +90,11 @@ struct Layout {
 struct PfTab {
   int L[kPfTable];        // context_lens
   int qs[kPfTable + 1];   // query_start
+  int parts[kPfTable];    // query tiles of the sequence (prefill_parts)
 };
 
-constexpr int kMiscBytes = 1280;          // single kernel
-constexpr int kMiscBytesPair = 1280;      // paired kernel
+constexpr int kMiscBytes = 1792;          // single kernel
+constexpr int kMiscBytesPair = 1792;      // paired kernel
 struct MiscPair {
   uint64_t k_full[Layout<true>::NK], k_empty[Layout<true>::NK], v_full[NV], v_empty[NV];
   // per slot (A, B)
@@ -158,10 +159,11 @@ __device__ __forceinline__ UnitInfo unit_at(const PfTab& tab, const DecodeArgs& 
   ui.slot = -1;
   const bool in_tab = a.num_seqs <= kPfTable;
   ui.L = in_tab ? tab.L[s] : a.context_lens[s];
-  ui.lok = len_ok(ui.L, a.max_context_len, a.max_blocks_per_seq, a.block_size);
   const int q0 = in_tab ? tab.qs[s] : a.query_start[s];
   const int q1 = in_tab ? tab.qs[s + 1] : a.query_start[s + 1];
-  if (p < prefill_parts(a, q0, q1, ui.L)) {
+  const int parts = in_tab ? tab.parts[s] : prefill_parts(a, q0, q1, ui.L);
+  ui.lok = parts > 0;
+  if (p < parts) {
     const int n = q1 - q0, i0 = p * a.q_per_unit;
     ui.nq = min(a.q_per_unit, n - i0);
     ui.qrow0 = q0 + i0;
@@ -182,8 +184,11 @@ __device__ __forceinline__ void prefill_setup(PfTab& tab, const DecodeArgs& a) {
   const int nthreads = blockDim.x;
   if (a.num_seqs <= kPfTable)
     for (int i = threadIdx.x; i <= a.num_seqs; i += nthreads) {
-      if (i < a.num_seqs) tab.L[i] = a.context_lens[i];
       tab.qs[i] = a.query_start[i];
+      if (i < a.num_seqs) {
+        tab.L[i] = a.context_lens[i];
+        tab.parts[i] = prefill_parts(a, a.query_start[i], a.query_start[i + 1], a.context_lens[i]);
+      }
     }
   for (int sq = blockIdx.x; sq < a.num_seqs; sq += gridDim.x) {
     const int L = a.context_lens[sq];
@@ -203,21 +208,38 @@ __device__ __forceinline__ void prefill_setup(PfTab& tab, const DecodeArgs& a) {
 // Units of one CTA: unit u of S * Hk * P, dealt round-robin (consecutive
 // query tiles of a causal chunk differ in cost; dealing spreads them), later
 // (heavier) tiles first.
-struct SingleCursor {
-  long long next, end;
-  int stride;
-  __device__ __forceinline__ void begin(const DecodeArgs& a) {
-    next = blockIdx.x;
-    stride = gridDim.x;
-    end = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
+// Round-robin walk over unit indices v = blockIdx.x + k * gridDim.x, v =
+// (s * Hk + hk) * per + r, kept as its parts (r, hk, s) while s < S: one
+// step adds the stride's parts (from the launch arguments) with carries, no
+// division.
+struct UnitWalk {
+  int r, hk, s;
+  __device__ __forceinline__ void begin(const DecodeArgs& a, int per) {
+    const int v = blockIdx.x;
+    r = v % per;
+    hk = (v / per) % a.num_kv_heads;
+    s = (v / per) / a.num_kv_heads;
   }
+  __device__ __forceinline__ bool more(const DecodeArgs& a) const { return s < a.num_seqs; }
+  __device__ __forceinline__ void advance(const DecodeArgs& a, int per) {
+    r += a.walk_dr;
+    const int c = r >= per;
+    if (c) r -= per;
+    hk += a.walk_dhk + c;
+    const int c2 = hk >= a.num_kv_heads;
+    if (c2) hk -= a.num_kv_heads;
+    s += a.walk_ds + c2;
+  }
+};
+
+struct SingleCursor {
+  UnitWalk w;
+  __device__ __forceinline__ void begin(const DecodeArgs& a) { w.begin(a, a.num_partitions); }
   __device__ __forceinline__ bool step(const PfTab& tab, const DecodeArgs& a, UnitInfo& ui) {
     const int per = a.num_partitions;
-    while (next < end) {
-      const int v = (int)next;
-      next += stride;
-      const int pp = per - 1 - v % per, sh = v / per;
-      const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
+    while (w.more(a)) {
+      const int pp = per - 1 - w.r, hk = w.hk, s = w.s;
+      w.advance(a, per);
       ui = unit_at(tab, a, s, hk, pp);
       if (ui.ntiles) return true;
     }
@@ -642,20 +664,13 @@ struct PairUnit {
 // (consecutive query tiles of a causal chunk differ in cost; dealing spreads
 // them), later (heavier) pairs first.
 struct PairCursor {
-  long long next, end;
-  int stride, per;
-  __device__ __forceinline__ void begin(const DecodeArgs& a) {
-    per = (a.num_partitions + 1) / 2;
-    next = blockIdx.x;
-    stride = gridDim.x;
-    end = (long long)a.num_seqs * a.num_kv_heads * per;
-  }
+  UnitWalk w;
+  __device__ __forceinline__ void begin(const DecodeArgs& a) { w.begin(a, (a.num_partitions + 1) / 2); }
   __device__ __forceinline__ bool step(const PfTab& tab, const DecodeArgs& a, PairUnit& pu) {
-    while (next < end) {
-      const int v = (int)next;
-      next += stride;
-      const int pp = per - 1 - v % per, sh = v / per;
-      const int hk = sh % a.num_kv_heads, s = sh / a.num_kv_heads;
+    const int per = (a.num_partitions + 1) / 2;
+    while (w.more(a)) {
+      const int pp = per - 1 - w.r, hk = w.hk, s = w.s;
+      w.advance(a, per);
       const UnitInfo ua = unit_at(tab, a, s, hk, 2 * pp);
       if (ua.ntiles == 0) continue;   // no tile 2pp, so no tile 2pp + 1 either
       const UnitInfo ub = unit_at(tab, a, s, hk, 2 * pp + 1);
@@ -1102,17 +1117,16 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
                                             ((size_t)(valid ? pu.qrow0[x] + qi : 0) * H +
                                              pu.hk * g + hj) * HD);
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        float v[32];
-        tmem_ld32(o_addr + c * 32, v);
+      {
+        float v[HD];   // the row of O in one TMEM load (the logits are dead here)
+        tmem_ld128(o_addr, v);
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[c * 4 + i] = make_uint4(pack2<BF16>(v[8 * i] * inv, v[8 * i + 1] * inv),
-                                        pack2<BF16>(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
-                                        pack2<BF16>(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
-                                        pack2<BF16>(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+          for (int i = 0; i < HD / 8; ++i)
+            dst[i] = make_uint4(pack2<BF16>(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                pack2<BF16>(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                pack2<BF16>(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                pack2<BF16>(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
         }
       }
       tc_fence_before();
@@ -1170,12 +1184,16 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   const bool pair = a.num_partitions >= 2 && a.max_context_len - a.max_query_len / 2 >= kPairMinTokens;
   cudaError_t e = pair ? prepare<BF16, true>() : prepare<BF16, false>();
   if (e != cudaSuccess) return e;
-  const long long units =
-      (long long)a.num_seqs * a.num_kv_heads * (pair ? (a.num_partitions + 1) / 2 : a.num_partitions);
+  const int per = pair ? (a.num_partitions + 1) / 2 : a.num_partitions;
+  const long long units = (long long)a.num_seqs * a.num_kv_heads * per;
   const int grid = (int)(units < sms ? units : sms);
+  DecodeArgs la = a;
+  la.walk_dr = grid % per;
+  la.walk_dhk = (grid / per) % a.num_kv_heads;
+  la.walk_ds = (grid / per) / a.num_kv_heads;
   return launch_pdl(pair ? prefill_pair_kernel<BF16> : prefill_single_kernel<BF16>, dim3(grid),
                     dim3(pair ? kThreadsPair : kThreads), pair ? smem_bytes<true>() : smem_bytes<false>(),
-                    st, km, vm, qm, a);
+                    st, km, vm, qm, la);
 }
 
 }  // namespace
