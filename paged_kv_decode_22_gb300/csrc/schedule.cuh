@@ -29,6 +29,10 @@ struct SchedSmem {
   int total;
   int L[kSchedMax];        // context length of each sequence
   int pre[kSchedMax + 1];  // units (stream: positions) of the sequences before s
+  // Stream form: this CTA's range [next, end) of the tile list and the
+  // (sequence, KV head, offset, positions per pair) of its first tile,
+  // found once by the set-up for every role's cursor.
+  int start[6];            // next, end, s, hk, off, np
 };
 
 struct UnitInfo {
@@ -82,10 +86,14 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
   c.s = c.hk = c.p = 0;
   c.np = -1;
   if (a.stream) {
-    // Stream form: an equal contiguous range of the sequence-major tile list.
-    const long long total = sc.total;
-    c.next = total * blockIdx.x / gridDim.x;
-    c.end = total * (blockIdx.x + 1) / gridDim.x;
+    // Stream form: an equal contiguous range of the sequence-major tile
+    // list, starting on the tile the set-up found.
+    c.next = sc.start[0];
+    c.end = sc.start[1];
+    c.s = sc.start[2];
+    c.hk = sc.start[3];
+    c.p = sc.start[4];
+    c.np = sc.start[5];
   } else if (a.fused) {
     // Cluster launch: grid (P, S * Hk), one unit per CTA, partition = x.
     c.next = (long long)blockIdx.y * a.num_partitions + blockIdx.x;
@@ -262,21 +270,34 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
       }
     }
     if (a.stream && warp == 0) {
-      // The pair cut by this CTA's left range edge, for the merge launch
-      // (warp 0 wrote the prefix).
+      // This CTA's range of the tile list and its first tile, for every
+      // role's cursor, and the pair cut by the range's left edge, for the
+      // merge launch (warp 0 wrote the prefix).
       __syncwarp();
       if (lane == 0) {
         const long long T = sc.total;
         const int t = (int)(T * blockIdx.x / gridDim.x);
-        int4 d = make_int4(0, 0, 0, (int)T);
-        if (blockIdx.x > 0 && t < T) {
-          int lo = 0, hi = a.num_seqs - 1;   // last s with pre[s] <= t
+        const int te = (int)(T * (blockIdx.x + 1) / gridDim.x);
+        int lo = 0, np = 1, hk = 0, off = 0;
+        if (t < T) {
+          int hi = a.num_seqs - 1;   // last s with pre[s] <= t (a sequence with entries)
           while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (sc.pre[mid] <= t) lo = mid; else hi = mid - 1;
           }
-          const int np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;
-          const int r = t - sc.pre[lo], hk = r / np, off = r - hk * np;
+          np = (sc.pre[lo + 1] - sc.pre[lo]) / a.num_kv_heads;
+          const int r = t - sc.pre[lo];
+          hk = r / np;
+          off = r - hk * np;
+        }
+        sc.start[0] = t;
+        sc.start[1] = te;
+        sc.start[2] = lo;
+        sc.start[3] = hk;
+        sc.start[4] = off;
+        sc.start[5] = np;
+        int4 d = make_int4(0, 0, 0, (int)T);
+        if (blockIdx.x > 0 && t < T) {
           const int nt = np - stream_pad(sc.L[lo]);
           if (off > 0 && off < nt)   // inside the pair's tiles
             d = make_int4(sc.pre[lo] + hk * np, nt, lo * a.num_kv_heads + hk, (int)T);
