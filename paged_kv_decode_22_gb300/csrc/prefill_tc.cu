@@ -82,7 +82,9 @@ struct Layout {
   static constexpr int off_q = 0;
   static constexpr int off_k = off_q + 2 * Q_BYTES;
   static constexpr int off_v = off_k + NK * TILE_BYTES;
-  static constexpr int off_misc = off_v + NV * TILE_BYTES;
+  // Single kernel: a query tile's output, staged for its TMA store.
+  static constexpr int off_stage = off_v + NV * TILE_BYTES;
+  static constexpr int off_misc = off_stage + (PAIR ? 0 : Q_BYTES);
 };
 
 // Lengths and chunk bounds, in shared memory when there are at most
@@ -110,6 +112,7 @@ static_assert(sizeof(MiscPair) <= kMiscBytesPair, "misc area too small");
 struct MiscSingle {
   uint64_t k_full[Layout<false>::NK], k_empty[Layout<false>::NK], v_full[NV], v_empty[NV];
   uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], pv_done[2], o_full[2], o_empty[2], drain;
+  uint64_t stage_full, stage_free;   // the output stage: rows written; read by the last store
   uint32_t tmem_base;
   int abort;
   int k_bad[Layout<false>::NK];      // per K stage: token offset of the tile's first bad block id, or -1
@@ -251,13 +254,15 @@ template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_single_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
-                      const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
+                      const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap omap, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   uint8_t* qbuf = sm + Layout<false>::off_q;
   uint8_t* kbuf = sm + Layout<false>::off_k;
   uint8_t* vbuf = sm + Layout<false>::off_v;
+  uint8_t* stage = sm + Layout<false>::off_stage;
   MiscSingle& ms = *reinterpret_cast<MiscSingle*>(sm + Layout<false>::off_misc);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -289,10 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ms.o_empty[i], kSoftmaxThreads);
     }
     mbar_init(&ms.drain, 1);
+    mbar_init(&ms.stage_full, kSoftmaxThreads);
+    mbar_init(&ms.stage_free, 1);
     ms.abort = 0;
     fence_barrier_init();
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&omap);
     tma_prefetch_desc(&qmap);
   }
   if (warp == 2) {
@@ -482,29 +490,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // A unit's output is written after the next unit's first P, so its last
     // P V runs while that tile's softmax does: the pending write's state.
-    bool pend = false, pend_valid = false;
-    int pend_ub = 0;
+    bool pend = false, pend_valid = false, pend_whole = false;
+    int pend_ub = 0, pend_hk = 0, pend_qrow0 = 0;
     float pend_inv = 0.f;
     uint4* pend_dst = nullptr;
+    // A unit's output rows.  A whole query tile goes through shared memory:
+    // each thread writes its row there (128-byte swizzled, the layout of the
+    // output tensor map's two {64, g, QT} boxes) and one thread stores the
+    // tile with two TMA stores, so the warpgroup's load/store path is not
+    // left with 16 global stores a thread in front of its next waits.  A
+    // partial tile (the end of a chunk) is written row by row.
+    uint32_t n_whole = 0;   // whole tiles stored through the stage
     auto finalize = [&]() {
       ok = ok && mbar_wait(&ms.o_full[pend_ub], (u_fin >> 1) & 1);
       if (!ok) return;
       tc_fence_after();
+      if (pend_whole) {
+        // The stage is free once the previous tile's store has read it.
+        if (threadIdx.x == 128) {
+          bulk_wait_read_all();
+          mbar_arrive(&ms.stage_free);
+        }
+        ok = mbar_wait(&ms.stage_free, n_whole & 1);
+        if (!ok) return;
+      }
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         float v[32];
         tmem_ld32(lane_addr + 256 + pend_ub * 128 + c * 32, v);
-        if (pend_valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            pend_dst[c * 4 + i] = make_uint4(pack2<BF16>(v[8 * i] * pend_inv, v[8 * i + 1] * pend_inv),
-                                             pack2<BF16>(v[8 * i + 2] * pend_inv, v[8 * i + 3] * pend_inv),
-                                             pack2<BF16>(v[8 * i + 4] * pend_inv, v[8 * i + 5] * pend_inv),
-                                             pack2<BF16>(v[8 * i + 6] * pend_inv, v[8 * i + 7] * pend_inv));
+        for (int i = 0; i < 4; ++i) {
+          const uint4 w = make_uint4(pack2<BF16>(v[8 * i] * pend_inv, v[8 * i + 1] * pend_inv),
+                                     pack2<BF16>(v[8 * i + 2] * pend_inv, v[8 * i + 3] * pend_inv),
+                                     pack2<BF16>(v[8 * i + 4] * pend_inv, v[8 * i + 5] * pend_inv),
+                                     pack2<BF16>(v[8 * i + 6] * pend_inv, v[8 * i + 7] * pend_inv));
+          if (pend_whole) {
+            // 16-byte chunk ch of this row's 64-column half (c >> 1).
+            const int ch = (c & 1) * 4 + i;
+            *reinterpret_cast<uint4*>(stage + (c >> 1) * Q_BYTES / 2 + row * 128 +
+                                      ((ch ^ (row & 7)) << 4)) = w;
+          } else if (pend_valid) {
+            pend_dst[c * 4 + i] = w;
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&ms.o_empty[pend_ub]);
+      if (pend_whole) {
+        fence_proxy_async_smem();   // the stage's writes, before the TMA reads them
+        mbar_arrive(&ms.stage_full);
+        if (threadIdx.x == 128) {
+          ok = mbar_wait(&ms.stage_full, n_whole & 1);
+          if (ok) {
+            tma_store_3d(&omap, stage, 0, pend_hk * g, pend_qrow0);
+            tma_store_3d(&omap, stage + Q_BYTES / 2, 64, pend_hk * g, pend_qrow0);
+            bulk_commit();
+          }
+        }
+        ++n_whole;
+      }
       pend = false;
       ++u_fin;
     };
@@ -634,12 +678,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       pend = true;
       pend_ub = ub;
       pend_valid = valid_row;
+      pend_whole = ui.nq == a.q_per_unit;
+      pend_hk = ui.hk;
+      pend_qrow0 = ui.qrow0;
       pend_inv = !valid_row || pos >= bad_from || l == 0.f ? 0.f : 1.f / l;
       pend_dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
                                           ((size_t)(ui.qrow0 + qi) * H + ui.hk * g + hj) * HD);
       ++u;
     }
     if (ok && pend) finalize();
+    if (threadIdx.x == 128) bulk_wait_all();   // every output store done before the CTA exits
     if (!ok && threadIdx.x == 128) set_abort(ms, a.status);
   }
 
@@ -1152,8 +1200,10 @@ cudaError_t prepare() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(PAIR ? prefill_pair_kernel<BF16> : prefill_single_kernel<BF16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<PAIR>());
+    e = PAIR ? cudaFuncSetAttribute(prefill_pair_kernel<BF16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<true>())
+             : cudaFuncSetAttribute(prefill_single_kernel<BF16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<false>());
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
@@ -1191,9 +1241,14 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   la.walk_dr = grid % per;
   la.walk_dhk = (grid / per) % a.num_kv_heads;
   la.walk_ds = (grid / per) / a.num_kv_heads;
-  return launch_pdl(pair ? prefill_pair_kernel<BF16> : prefill_single_kernel<BF16>, dim3(grid),
-                    dim3(pair ? kThreadsPair : kThreads), pair ? smem_bytes<true>() : smem_bytes<false>(),
-                    st, km, vm, qm, la);
+  if (pair)
+    return launch_pdl(prefill_pair_kernel<BF16>, dim3(grid), dim3(kThreadsPair), smem_bytes<true>(),
+                      st, km, vm, qm, la);
+  CUtensorMap om;   // the output, boxes like the query tiles'
+  if (!make_q_chunk_map(&om, a.out, BF16, HD, a.num_heads, a.num_q_tokens, g, a.q_per_unit))
+    return cudaErrorInvalidValue;
+  return launch_pdl(prefill_single_kernel<BF16>, dim3(grid), dim3(kThreads), smem_bytes<false>(), st,
+                    km, vm, qm, om, la);
 }
 
 }  // namespace

@@ -176,6 +176,18 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
       : "memory");
 }
 
+// Tiled TMA store shared -> global (3-D box at {x, y, z}), tracked by bulk
+// groups like bulk_store.  x * element size must be a multiple of 16 bytes,
+// and no coordinate may be negative.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src_smem, int x,
+                                             int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          map),
+      "r"(smem_u32(src_smem)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // Bulk copy shared -> global (no tensor map), tracked by bulk groups.
 // Addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
