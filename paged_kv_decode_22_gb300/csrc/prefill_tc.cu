@@ -250,7 +250,29 @@ struct SingleCursor {
   }
 };
 
-template <bool BF16>
+// A row's logits x of the tile at token ts, in log2 units and masked past
+// the query's position pos.  When the scale folds into the exponent's FMA
+// (fold: no ALiBi and a scale above 0) only a tile that passes the query is
+// touched; otherwise each visible logit is scaled and gets the bias slope *
+// (t - pos) (slope 0 without ALiBi).  FOLD instantiates a kernel for the
+// folded case alone (the host launches it for exactly that case), so the
+// common kernel carries no bias code in the loop that every tile runs.
+template <bool FOLD>
+__device__ __forceinline__ void mask_logits(float (&x)[TT], bool fold, float qscale, float slope,
+                                            int ts, int pos) {
+  if (!FOLD && !fold) {
+#pragma unroll
+    for (int i = 0; i < TT; ++i) {
+      const int t = ts + i;
+      x[i] = t <= pos ? fmaf(x[i], qscale, slope * (float)(t - pos)) : -INFINITY;
+    }
+  } else if (ts + TT - 1 > pos) {            // the tile passes this row's query
+#pragma unroll
+    for (int i = 0; i < TT; ++i) x[i] = ts + i <= pos ? x[i] : -INFINITY;
+  }
+}
+
+template <bool BF16, bool FOLD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_single_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
@@ -572,21 +594,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // This row's logits for the tile, log2 units, masked past the query.
         float x[TT];
         tmem_ld128(lane_addr + b * 128, x);
-        // Logits in log2 units are x * sc: without ALiBi the scale folds into
-        // the exponent's FMA (sc = scale * log2 e > 0: the maximum of x is the
-        // maximum of the logits); with ALiBi x carries the scale and the bias.
-        const bool fold = !alibi && qscale > 0.f;
+        // Logits in log2 units are x * sc: folded (no ALiBi, sc = scale *
+        // log2 e > 0: the maximum of x is the maximum of the logits), or x
+        // carries the scale and the bias.
+        const bool fold = FOLD || (!alibi && qscale > 0.f);
         const float sc = fold ? qscale : 1.f;
-        if (!fold) {
-#pragma unroll
-          for (int i = 0; i < TT; ++i) {
-            const int t = ts + i;
-            x[i] = t <= pos ? fmaf(x[i], qscale, slope * (float)(t - pos)) : -INFINITY;
-          }
-        } else if (ts + TT - 1 > pos) {         // the tile passes this row's query
-#pragma unroll
-          for (int i = 0; i < TT; ++i) x[i] = ts + i <= pos ? x[i] : -INFINITY;
-        }
+        mask_logits<FOLD>(x, fold, qscale, slope, ts, pos);
         // Row maximum: 8 independent chains of three-input maxima, then a
         // tree.
         float m8[8];
@@ -740,7 +753,7 @@ struct PairCursor {
   }
 };
 
-template <bool BF16>
+template <bool BF16, bool FOLD>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap,
@@ -1016,7 +1029,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     const int H = a.num_heads;
     const int qi = row / g, hj = row - qi * g; // row = (tile query qi, head hj of the group)
     const bool alibi = a.alibi != nullptr;
-    const bool fold = !alibi && qscale > 0.f;
+    const bool fold = FOLD || (!alibi && qscale > 0.f);
     const float sc = fold ? qscale : 1.f;
     uint32_t j = 0, jx = 0, ux = 0;            // tiles of all units, tiles and units of this slot
     bool ok = true;
@@ -1055,24 +1068,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         ok = ok && mbar_wait(&ms.s_full[x], jx & 1);
         if (!ok) break;
         tc_fence_after();
-        // This row's logits for the tile, log2 units, masked past the query,
-        // one 64-column half at a time: the second half for its maximum, the
-        // first (kept) for its maximum and exponentials, then the second
-        // again.  Without ALiBi the scale folds into the exponent's FMA (sc =
-        // scale * log2 e > 0: the maximum of xv is the maximum of the
-        // logits); with ALiBi xv carries the scale and the bias.
+        // This row's logits for the tile in one TMEM load, log2 units,
+        // masked past the query: folded (no ALiBi, sc = scale * log2 e > 0:
+        // the maximum of xv is the maximum of the logits), or xv carries the
+        // scale and the bias.
         float xv[TT];
         tmem_ld128(s_addr, xv);
-        if (!fold) {
-#pragma unroll
-          for (int i = 0; i < TT; ++i) {
-            const int t = ts + i;
-            xv[i] = t <= pos ? fmaf(xv[i], qscale, slope * (float)(t - pos)) : -INFINITY;
-          }
-        } else if (ts + TT - 1 > pos) {         // the tile passes this row's query
-#pragma unroll
-          for (int i = 0; i < TT; ++i) xv[i] = ts + i <= pos ? xv[i] : -INFINITY;
-        }
+        mask_logits<FOLD>(xv, fold, qscale, slope, ts, pos);
         float m8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) m8[k] = fmaxf(xv[k], xv[8 + k]);
@@ -1193,16 +1195,16 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
 }
 
 // Maximum dynamic shared memory, set once per device and kernel.
-template <bool BF16, bool PAIR>
+template <bool BF16, bool FOLD, bool PAIR>
 cudaError_t prepare() {
   static std::atomic<bool> attr_set[64];   // setting it twice from two threads is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
-    e = PAIR ? cudaFuncSetAttribute(prefill_pair_kernel<BF16>,
+    e = PAIR ? cudaFuncSetAttribute(prefill_pair_kernel<BF16, FOLD>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<true>())
-             : cudaFuncSetAttribute(prefill_single_kernel<BF16>,
+             : cudaFuncSetAttribute(prefill_single_kernel<BF16, FOLD>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<false>());
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
@@ -1218,7 +1220,7 @@ cudaError_t prepare() {
 // 256-token chunk after 3840 cached tokens runs in 149 us against 171 on the
 // single kernel, while 1024-token prompts without prefix ran 237 -> 298 us
 // on the paired kernel's first version.
-template <bool BF16>
+template <bool BF16, bool FOLD>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   CUtensorMap km, vm, qm;
   const long long rows = (long long)a.num_blocks * a.block_size;
@@ -1232,7 +1234,7 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool pair = a.num_partitions >= 2 && a.max_context_len - a.max_query_len / 2 >= kPairMinTokens;
-  cudaError_t e = pair ? prepare<BF16, true>() : prepare<BF16, false>();
+  cudaError_t e = pair ? prepare<BF16, FOLD, true>() : prepare<BF16, FOLD, false>();
   if (e != cudaSuccess) return e;
   const int per = pair ? (a.num_partitions + 1) / 2 : a.num_partitions;
   const long long units = (long long)a.num_seqs * a.num_kv_heads * per;
@@ -1242,12 +1244,12 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
   la.walk_dhk = (grid / per) % a.num_kv_heads;
   la.walk_ds = (grid / per) / a.num_kv_heads;
   if (pair)
-    return launch_pdl(prefill_pair_kernel<BF16>, dim3(grid), dim3(kThreadsPair), smem_bytes<true>(),
+    return launch_pdl(prefill_pair_kernel<BF16, FOLD>, dim3(grid), dim3(kThreadsPair), smem_bytes<true>(),
                       st, km, vm, qm, la);
   CUtensorMap om;   // the output, boxes like the query tiles'
   if (!make_q_chunk_map(&om, a.out, BF16, HD, a.num_heads, a.num_q_tokens, g, a.q_per_unit))
     return cudaErrorInvalidValue;
-  return launch_pdl(prefill_single_kernel<BF16>, dim3(grid), dim3(kThreads), smem_bytes<false>(), st,
+  return launch_pdl(prefill_single_kernel<BF16, FOLD>, dim3(grid), dim3(kThreads), smem_bytes<false>(), st,
                     km, vm, qm, om, la);
 }
 
@@ -1259,7 +1261,11 @@ cudaError_t launch_prefill_rows(const DecodeArgs& a, cudaStream_t st) {
   const int g = a.num_heads / a.num_kv_heads;
   if (a.head_size != HD || g < 1 || g > 64 || a.q_per_unit != prefill_rows_queries_per_unit(g))
     return cudaErrorInvalidValue;
-  return a.is_bf16 ? launch_t<true>(a, st) : launch_t<false>(a, st);
+  // The scale folds into the exponent's FMA when it is above 0 and there is
+  // no bias.
+  if (a.alibi == nullptr && a.scale > 0.f)
+    return a.is_bf16 ? launch_t<true, true>(a, st) : launch_t<false, true>(a, st);
+  return a.is_bf16 ? launch_t<true, false>(a, st) : launch_t<false, false>(a, st);
 }
 
 }  // namespace pkd

@@ -48,7 +48,7 @@ FORM_CTX = {"single": None, "pair": 8192}
 
 
 def _run(c, *, max_query_len=None, max_context_len=None, block_tables=None, context_lens=None,
-         alibi=None, form="single"):
+         alibi=None, form="single", scale=None):
     if max_context_len is None:
         max_context_len = FORM_CTX[form]
     from paged_kv_decode_22_gb300 import ops
@@ -60,17 +60,17 @@ def _run(c, *, max_query_len=None, max_context_len=None, block_tables=None, cont
         up(b.block_tables if block_tables is None else block_tables),
         up(b.context_lens if context_lens is None else context_lens), up(c.query_start),
         int(c.query_lens.max()) if max_query_len is None else max_query_len,
-        b.max_context_len if max_context_len is None else max_context_len, b.scale,
-        device_status=status,
+        b.max_context_len if max_context_len is None else max_context_len,
+        b.scale if scale is None else scale, device_status=status,
         alibi_slopes=None if alibi is None else torch.from_numpy(alibi).cuda())
     torch.cuda.synchronize()
     return decode_bits(down_bits(out), b.dtype), int(status.item())
 
 
-def _oracle(c, **kw):
+def _oracle(c, scale=None, **kw):
     b = c.base
     return oracle_prefill(c.q, b.key_cache, b.value_cache, b.block_tables, b.context_lens,
-                          c.query_start, b.scale, b.dtype, **kw)
+                          c.query_start, b.scale if scale is None else scale, b.dtype, **kw)
 
 
 @pytest.mark.parametrize("form", ["single", "pair"])
@@ -112,6 +112,18 @@ def test_prefill_with_alibi(H, Hk, B, dtype, form):
     assert status == 0
     assert_close_ulp(got, _oracle(c, alibi_slopes=slopes.astype(np.float64)), dtype,
                      "prefill alibi")
+
+
+@pytest.mark.parametrize("form", ["single", "pair"])
+@pytest.mark.parametrize("scale", [0.0, -0.06])
+def test_prefill_with_a_scale_of_zero_or_below(scale, form):
+    # Such a scale cannot fold into the exponent (the maximum of the scaled
+    # logits is then not the scaled maximum), so these calls run in the
+    # kernel instantiation that scales every logit first, the one ALiBi uses.
+    c = _case(71, 64, 8, 16, "bf16", [(400, 150), (1500, 256), (33, 1)])
+    got, status = _run(c, form=form, scale=scale)
+    assert status == 0
+    assert_close_ulp(got, _oracle(c, scale=scale), "bf16", f"prefill scale {scale}")
 
 
 def test_one_query_per_sequence_equals_decode():
