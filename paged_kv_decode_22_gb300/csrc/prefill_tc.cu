@@ -43,6 +43,10 @@
 // producers' path from a stage's release to its TMA issue holds no warp
 // exchange.  A unit whose second tile does not exist (the last of an odd
 // count) runs slot A only.
+// Each kernel has two instantiations: FOLD (no ALiBi, scale above 0: the
+// scale folds into the exponent's FMA and only tiles that pass a query are
+// masked) and the general one (every logit scaled, ALiBi bias added), so
+// the loop that every tile runs in the common case holds no bias code.
 #include <cuda.h>
 
 #include <atomic>
