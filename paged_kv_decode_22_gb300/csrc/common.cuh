@@ -9,18 +9,6 @@
 
 namespace pkd {
 
-// Two 16-bit values packed in a 32-bit word, widened to float.
-template <bool BF16>
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-  if constexpr (BF16) {
-    // bf16 is the top half of a binary32: widening is a shift, exact.
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-  } else {
-    __half2 h = *reinterpret_cast<__half2*>(&w);
-    return __half22float2(h);
-  }
-}
-
 // Round two floats to the 16-bit format (nearest-even) and pack them.
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
