@@ -145,7 +145,7 @@ __device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
   return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
 }
 
-template <bool BF16, int NPAD>
+template <bool BF16, int NPAD, int FORM>
 __global__ void __launch_bounds__(threads_of(NPAD), 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   const int g = a.num_heads / a.num_kv_heads;
 
   // ---------------------------------------------------------------- setup
-  prefetch_schedule_inputs(a);
+  prefetch_schedule_inputs<FORM>(a);
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) {
       mbar_init(&ms.k_full[i], 1);
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   }
   pdl_wait();
   pdl_launch_dependents();
-  schedule_setup(ms.sched, a, kThreads);
+  schedule_setup<FORM>(ms.sched, a, kThreads);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -238,9 +238,9 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       }
       return raw;
     };
-    UnitCursor cur = cursor_begin(ms.sched, a);
+    UnitCursor cur = cursor_begin<FORM>(ms.sched, a);
     UnitInfo ui;
-    bool have = cursor_next<TT>(cur, ms.sched, a, ui);
+    bool have = cursor_next<TT, FORM>(cur, ms.sched, a, ui);
     int jl = 0;
     int raw = have ? load_raw(ui, 0) : kNoBlock;
     uint32_t jk = 0, un = 0;
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       bool nhave = true;
       int njl = jl + 1;
       if (njl >= ui.ntiles) {
-        nhave = cursor_next<TT>(cur, ms.sched, a, nui);
+        nhave = cursor_next<TT, FORM>(cur, ms.sched, a, nui);
         njl = 0;
       }
       const int nraw = nhave ? load_raw(nui, njl) : kNoBlock;
@@ -326,9 +326,9 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         mma_commit(&ms.o_full[b]);
         mma_commit(&ms.v_empty[vs]);
       };
-      UnitCursor cur = cursor_begin(ms.sched, a);
+      UnitCursor cur = cursor_begin<FORM>(ms.sched, a);
       UnitInfo ui;
-      while (ok && cursor_next<TT>(cur, ms.sched, a, ui)) {
+      while (ok && cursor_next<TT, FORM>(cur, ms.sched, a, ui)) {
         // The softmax warps finish the previous unit only after its last P V:
         // issue that one before this unit's first S.
         if (prev >= 0) {
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float qscale = a.scale * kLog2e;
     const bool single = a.num_partitions == 1;
-    const bool fused = a.fused != 0;           // one unit, merged over the cluster
+    const bool fused = form_fused<FORM>(a);    // one unit, merged over the cluster
     const int H = a.num_heads;
     const int group_heads = max(0, min(HPG, g - hbase));    // decode: valid heads of this warpgroup
     // This thread's element (column hbase + hl, token row) of the K-major,
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       tc_fence_before();
     };
 
-    UnitCursor cur = cursor_begin(ms.sched, a);
+    UnitCursor cur = cursor_begin<FORM>(ms.sched, a);
     UnitInfo ui, nx;
     const bool alibi = a.alibi != nullptr;
     // Per-unit state of this warpgroup's columns in buffer ub: reference
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
         if (alibi && et < group_heads) ms.slope[ub][c] = a.alibi[v.hk * g + c] * kLog2e;
       }
     };
-    bool have = cursor_next<TT>(cur, ms.sched, a, ui);
+    bool have = cursor_next<TT, FORM>(cur, ms.sched, a, ui);
     if (have) setup_unit(ui, 0);
     named_barrier(bar, kSoftmaxThreads);
     uint32_t u = 0;                    // units done by this warpgroup
@@ -571,9 +571,9 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
       // Workspace or cluster partial (unnormalised), or a whole result.  In
       // the stream form a unit cut by the CTA's range edge is a partial in
       // its slot; every other unit is whole.
-      const bool partial = a.stream ? ui.slot >= 0 : !single;
+      const bool partial = form_stream<FORM>(a) ? ui.slot >= 0 : !single;
       const size_t unit_row =
-          a.stream ? (size_t)ui.slot * g
+          form_stream<FORM>(a) ? (size_t)ui.slot * g
                    : (((size_t)ui.s * a.num_kv_heads + ui.hk) * a.num_partitions + ui.p) * g;
       if (partial) {
         if (fused) {
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
             if (hl < my_heads) wo[hl * HD] = o_acc[hl];
         }
       }
-      const bool have_next = cursor_next<TT>(cur, ms.sched, a, nx);
+      const bool have_next = cursor_next<TT, FORM>(cur, ms.sched, a, nx);
       if (have_next) setup_unit(nx, ub ^ 1);
       {
         const float t = warp_sum16(l_part, lane);
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(threads_of(NPAD), 1)
   // and the sums l (negative for a bad block).  Heads are dealt round-robin
   // to the ranks; a warp merges one head, each lane 4 columns of d:
   //     M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
-  if (a.fused) {
+  if (form_fused<FORM>(a)) {
     cluster_sync();
     constexpr int HPG = NPAD / GROUPS, PER = HPG / 4;   // staging: PER rows per piece
     const int P = a.num_partitions;
@@ -709,7 +709,7 @@ int pad_group(int g) { return (g + 15) / 16 * 16; }
 
 // Kernel attributes, set once per device: the dynamic shared memory and
 // clusters of up to 16 CTAs.
-template <bool BF16, int NPAD>
+template <bool BF16, int NPAD, int FORM>
 cudaError_t prepare(int* smem_out) {
   const int smem = SmemLayout<NPAD>::bytes + 1024;
   *smem_out = smem;
@@ -718,9 +718,9 @@ cudaError_t prepare(int* smem_out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || attr_set[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
+  if ((e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD, FORM>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD>,
+      (e = cudaFuncSetAttribute(decode_tc_kernel<BF16, NPAD, FORM>,
                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
     return e;
   attr_set[dev].store(true, std::memory_order_release);
@@ -754,23 +754,29 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
       !make_rows_map(&qm, a.q, BF16, HD, (long long)a.num_seqs * a.num_heads, 64, NPAD))
     return cudaErrorInvalidValue;
   int smem = 0;
-  cudaError_t e = prepare<BF16, NPAD>(&smem);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   if (a.fused) {
     // One cluster of P CTAs per (sequence, KV head).
+    if ((e = prepare<BF16, NPAD, kFormCluster>(&smem)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     cluster_config(&cfg, attr, dim3(a.num_partitions, a.num_seqs * a.num_kv_heads),
                    threads_of(NPAD), smem, a.num_partitions, st);
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BF16, NPAD>, km, vm, qm, a);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<BF16, NPAD, kFormCluster>, km, vm, qm, a);
   }
+  if (a.stream) {
+    if ((e = prepare<BF16, NPAD, kFormStream>(&smem)) != cudaSuccess) return e;
+    return launch_pdl(decode_tc_kernel<BF16, NPAD, kFormStream>, dim3(a.stream_ctas),
+                      dim3(threads_of(NPAD)), smem, st, km, vm, qm, a);
+  }
+  if ((e = prepare<BF16, NPAD, kFormPlain>(&smem)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long units = (long long)a.num_seqs * a.num_kv_heads * a.num_partitions;
-  const int grid = a.stream ? a.stream_ctas : (int)(units < sms ? units : sms);
-  return launch_pdl(decode_tc_kernel<BF16, NPAD>, dim3(grid), dim3(threads_of(NPAD)), smem, st,
-                    km, vm, qm, a);
+  const int grid = (int)(units < sms ? units : sms);
+  return launch_pdl(decode_tc_kernel<BF16, NPAD, kFormPlain>, dim3(grid), dim3(threads_of(NPAD)),
+                    smem, st, km, vm, qm, a);
 }
 
 // Co-resident clusters of `cluster` CTAs, cached per device and cluster size.
@@ -782,11 +788,11 @@ int capacity_t(int cluster) {
   std::atomic<int>& c = cache[dev][cluster];
   if (c.load(std::memory_order_relaxed) == 0) {
     int smem = 0, n = 0;
-    if (prepare<true, NPAD>(&smem) == cudaSuccess) {
+    if (prepare<true, NPAD, kFormCluster>(&smem) == cudaSuccess) {
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr[2];
       cluster_config(&cfg, attr, dim3(cluster), threads_of(NPAD), smem, cluster, nullptr);
-      if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<true, NPAD>, &cfg) !=
+      if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<true, NPAD, kFormCluster>, &cfg) !=
           cudaSuccess) {
         cudaGetLastError();   // a refused query only means "no cluster launch"
         n = 0;

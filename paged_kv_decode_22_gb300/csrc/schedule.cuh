@@ -25,6 +25,20 @@ namespace pkd {
 
 constexpr int kSchedMax = 1024;
 
+// The split-context form of a decode launch: read from the arguments at run
+// time, or fixed by a kernel instantiation, so that an instantiation holds
+// only its own form's code (a kernel's instruction footprint is part of a
+// short call's time).
+constexpr int kFormRuntime = -1, kFormPlain = 0, kFormCluster = 1, kFormStream = 2;
+template <int FORM>
+__device__ __forceinline__ bool form_stream(const DecodeArgs& a) {
+  return FORM == kFormRuntime ? a.stream != 0 : FORM == kFormStream;
+}
+template <int FORM>
+__device__ __forceinline__ bool form_fused(const DecodeArgs& a) {
+  return FORM == kFormRuntime ? a.fused != 0 : FORM == kFormCluster;
+}
+
 struct SchedSmem {
   int total;
   int L[kSchedMax];        // context length of each sequence
@@ -80,12 +94,13 @@ struct UnitCursor {
                       // stream: position of the next tile (np = positions per pair of s)
 };
 
+template <int FORM = kFormRuntime>
 __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const DecodeArgs& a) {
   UnitCursor c;
-  c.dense = !a.fused && a.num_seqs <= kSchedMax;
+  c.dense = !form_fused<FORM>(a) && a.num_seqs <= kSchedMax;
   c.s = c.hk = c.p = 0;
   c.np = -1;
-  if (a.stream) {
+  if (form_stream<FORM>(a)) {
     // Stream form: an equal contiguous range of the sequence-major tile
     // list, starting on the tile the set-up found.
     c.next = sc.start[0];
@@ -94,7 +109,7 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
     c.hk = sc.start[3];
     c.p = sc.start[4];
     c.np = sc.start[5];
-  } else if (a.fused) {
+  } else if (form_fused<FORM>(a)) {
     // Cluster launch: grid (P, S * Hk), one unit per CTA, partition = x.
     c.next = (long long)blockIdx.y * a.num_partitions + blockIdx.x;
     c.end = c.next + 1;
@@ -109,10 +124,10 @@ __device__ __forceinline__ UnitCursor cursor_begin(const SchedSmem& sc, const De
   return c;
 }
 
-template <int TT>
+template <int TT, int FORM = kFormRuntime>
 __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
                                             const DecodeArgs& a, UnitInfo& ui) {
-  if (a.stream) {
+  if (form_stream<FORM>(a)) {
     // Units are the runs of the CTA's range over one pair's tiles; np =
     // positions per pair of sequence s (its tiles and empty positions).
     while (c.next < c.end) {
@@ -212,9 +227,10 @@ __device__ __forceinline__ bool cursor_next(UnitCursor& c, const SchedSmem& sc,
 // schedule, else a share) and, in the persistent forms, the used head of
 // every block-table row (ceil(max_context_len / block_size) entries), row s
 // by CTA s mod G; in the cluster form the CTA's own length and partition.
+template <int FORM = kFormRuntime>
 __device__ __forceinline__ void prefetch_schedule_inputs(const DecodeArgs& a) {
   const int S = a.num_seqs, B = a.block_size, mbps = a.max_blocks_per_seq;
-  if (a.fused) {
+  if (form_fused<FORM>(a)) {
     const int s = blockIdx.y / a.num_kv_heads;
     const long long b0 = (long long)blockIdx.x * a.partition_size / B;
     prefetch_l2_lines(a.context_lens + s, 4, 0, 1, 1);
@@ -238,9 +254,10 @@ __device__ __forceinline__ void prefetch_schedule_inputs(const DecodeArgs& a) {
 // have nothing to attend to (unsplit plans; the merge writes them when
 // split), setting the length status bit for invalid lengths.  Every thread
 // of the CTA calls this; it ends with __syncthreads().
+template <int FORM = kFormRuntime>
 __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& a, int nthreads) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (a.fused) {   // one unit per CTA; the cluster merge handles empty sequences
+  if (form_fused<FORM>(a)) {   // one unit per CTA; the cluster merge handles empty sequences
     __syncthreads();
     return;
   }
@@ -249,7 +266,7 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
       const int L = a.context_lens[i];
       sc.L[i] = L;
       const int n = parts_of(a, L);
-      sc.pre[i + 1] = (a.stream && n > 0 ? n + stream_pad(L) : n) * a.num_kv_heads;
+      sc.pre[i + 1] = (form_stream<FORM>(a) && n > 0 ? n + stream_pad(L) : n) * a.num_kv_heads;
     }
     __syncthreads();
     if (warp == 0) {
@@ -269,7 +286,7 @@ __device__ __forceinline__ void schedule_setup(SchedSmem& sc, const DecodeArgs& 
         sc.total = carry;
       }
     }
-    if (a.stream && warp == 0) {
+    if (form_stream<FORM>(a) && warp == 0) {
       // This CTA's range of the tile list and its first tile, for every
       // role's cursor, and the pair cut by the range's left edge, for the
       // merge launch (warp 0 wrote the prefix).
