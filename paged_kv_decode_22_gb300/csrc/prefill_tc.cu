@@ -540,7 +540,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&ms.stage_free, n_whole & 1);
         if (!ok) return;
       }
-#pragma unroll
+      // A rolled loop: this code runs once per unit, and unrolled it would
+      // take instruction-cache room from the loop every tile runs.
+#pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         float v[32];
         tmem_ld32(lane_addr + 256 + pend_ub * 128 + c * 32, v);
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = ok && mbar_wait(&ms.pv_done[jp & 1], (jp >> 1) & 1);
           tc_fence_after();
           const uint32_t o_addr = lane_addr + 256 + ub * 128;
-#pragma unroll
+#pragma unroll 1   // rare: kept out of the instruction cache's way
           for (int c = 0; c < HD / 32; ++c) {
             float v[32];
             uint32_t w[32];
