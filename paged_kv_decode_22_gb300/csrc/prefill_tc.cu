@@ -1127,7 +1127,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         if (__any_sync(0xffffffffu, alpha != 1.f && jl > 0)) {
           ok = ok && mbar_wait(&ms.pv_done[x], (jx - 1) & 1);
           tc_fence_after();
-#pragma unroll
+#pragma unroll 1   // rare: kept out of the instruction cache's way
           for (int c = 0; c < HD / 16; ++c) {
             float v[16];
             uint32_t w[16];
@@ -1173,16 +1173,19 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
                                             ((size_t)(valid ? pu.qrow0[x] + qi : 0) * H +
                                              pu.hk * g + hj) * HD);
-      {
-        float v[HD];   // the row of O in one TMEM load (the logits are dead here)
-        tmem_ld128(o_addr, v);
+      // A rolled loop over 32-column pieces: this runs once per unit, and
+      // unrolled it would take instruction-cache room from the tile loop.
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld32(o_addr + c * 32, v);
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < HD / 8; ++i)
-            dst[i] = make_uint4(pack2<BF16>(v[8 * i] * inv, v[8 * i + 1] * inv),
-                                pack2<BF16>(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
-                                pack2<BF16>(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
-                                pack2<BF16>(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+          for (int i = 0; i < 4; ++i)
+            dst[c * 4 + i] = make_uint4(pack2<BF16>(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                        pack2<BF16>(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                        pack2<BF16>(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                        pack2<BF16>(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
         }
       }
       tc_fence_before();
