@@ -95,6 +95,24 @@ def test_ragged_lengths_and_edges(H, Hk, D, B, dtype, partition_size):
     assert (got[lens.index(0)] == 0).all()
 
 
+@pytest.mark.parametrize("H,Hk,dtype", [(32, 4, "bf16"), (48, 1, "fp16"), (8, 8, "fp16")])
+@pytest.mark.parametrize("partition_size", [0, 64])
+def test_more_sequences_than_the_schedule_table_holds(H, Hk, dtype, partition_size):
+    # 1100 sequences: past the 1024 whose lengths the kernels keep in shared
+    # memory, units are dealt round-robin from lengths read in global memory
+    # (tensor-core groups), and the stream form is not offered.
+    from paged_kv_decode_22_gb300 import ops
+    lens = [int(L) for L in np.random.default_rng(41).integers(0, 200, 1100)]
+    c = _ragged(43, H, Hk, 128, 16, lens, dtype)
+    _, npart, path, _ = ops.decode_plan(c.num_seqs, H, Hk, 128, 16, c.max_context_len,
+                                        partition_size)
+    assert path != ops.PATH_TC_STREAM
+    got, status = run_decode(DeviceCase(c), partition_size=partition_size)
+    assert status == 0
+    assert_close(got, _oracle(c), f"1100 sequences H{H}/{Hk} {dtype} ps{partition_size} path {path}")
+    assert (got[np.asarray(lens) == 0] == 0).all()
+
+
 ALIBI = [(8, 8, 128, 16, "fp16"), (12, 4, 64, 32, "bf16"), (64, 8, 128, 16, "bf16"),
          (48, 1, 128, 16, "fp16"), (32, 1, 128, 64, "bf16")]
 
