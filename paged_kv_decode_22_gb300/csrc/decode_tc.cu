@@ -29,13 +29,17 @@
 // Shared-memory operands use the 128-byte swizzled canonical layouts: K, q and
 // P K-major, V MN-major (head_size contiguous).
 //
-// Split context comes in two forms.  Workspace form: each unit writes its
+// Split context comes in three forms.  Workspace form: each unit writes its
 // partial (o, m, l) to global memory and lse_reduce merges them in a second
 // launch.  Cluster form (small grids): the P partitions of one (sequence, KV
 // head) are the P CTAs of one thread-block cluster, one unit each; they keep
 // their partials in shared memory and merge them over distributed shared
 // memory before the kernel ends, so there is neither workspace nor merge
-// launch.
+// launch.  Stream form: every CTA takes an equal share of all tiles, and the
+// pairs cut at share edges are merged by a second launch.  The form is a
+// template argument (plain -- unsplit or workspace --, cluster, stream), so
+// each instantiation holds only its own form's code: on short calls the
+// instruction footprint is part of the time.
 #include <cuda.h>
 
 #include <atomic>
